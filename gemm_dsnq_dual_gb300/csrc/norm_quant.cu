@@ -1,0 +1,388 @@
+// Fused dual RMSNorm + per-1x128 FP8 group quant, the two unfused baseline
+// kernels it replaces, and the load-time 128x128 weight-block quantizer.
+//
+// Method: vLLM PR #53540 ("Purpose"): RMSNorm both MLA latents with fp32
+// accumulation and quantize the normalized q latent per 1x128 group to FP8
+// with fp32 scales in the same pass, reading the fp32 values (one rounding);
+// kv stays bf16.  Scale layout switch: sglang PR #27289 ("transpose_scale").
+//
+// Kernel shape (one CTA = one warp-group = one token row):
+//   * a row is cut into 16-byte chunks of 8 bf16; chunk c < Kq/8 is q, the
+//     rest is kv.  Thread t owns chunks t, t+128, ... (PASSES of them), so a
+//     DSv4 row (192 q chunks + 64 kv chunks) is exactly two 16-byte loads per
+//     thread, coalesced, from strided split views as well as contiguous rows;
+//   * the two sums of squares are reduced with warp shuffles and one
+//     cross-warp step through shared memory;
+//   * Kq is a multiple of 128, so in every pass each aligned half-warp holds
+//     exactly one 128-column q group (or kv, or nothing): the group amax is a
+//     4-step 16-lane shuffle, and lane 0 of the half-warp stores the scale;
+//   * codes are packed 8 per thread and stored as one 8-byte word, kv as one
+//     16-byte word.
+// The whole row stays in registers between the reductions and the stores, so
+// each input byte is read once and each output byte written once.
+
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+
+#include "dsnq_internal.h"
+
+namespace dsnq {
+
+constexpr int kThreads = 128;       // one warp-group per row
+constexpr int kChunk = 8;           // bf16 per 16-byte chunk
+constexpr float kE4M3Max = 448.0f;  // largest finite E4M3FN value
+
+enum Mode : int {
+    kFused = 0,      // q -> fp8 codes + scales, kv -> bf16
+    kNormOnly = 1,   // q -> bf16, kv -> bf16 (baseline step 1)
+    kQuantOnly = 2,  // x (passed as q) -> fp8 codes + scales, no norm (baseline step 2)
+};
+
+struct RowArgs {
+    const __nv_bfloat16* q;
+    const __nv_bfloat16* kv;
+    const __nv_bfloat16* gamma_q;
+    const __nv_bfloat16* gamma_kv;
+    int64_t ldq, ldkv;
+    int cq, ckv;           // chunk counts Kq/8, Kkv/8
+    float kq_f, kkv_f;     // Kq and Kkv as floats (divisors of the mean)
+    float eps;
+    uint8_t* q_fp8;        // kFused / kQuantOnly
+    __nv_bfloat16* q_bf16; // kNormOnly
+    int64_t ldq_out;
+    float* scale;
+    int64_t scale_row_stride, scale_group_stride;  // (m, g) at m*rs + g*gs
+    __nv_bfloat16* kv_out;
+    int64_t ldkv_out;
+};
+
+__device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float2 t = __bfloat1622float2(h[i]);
+        f[2 * i] = t.x;
+        f[2 * i + 1] = t.y;
+    }
+}
+
+__device__ __forceinline__ uint4 pack8_bf16(const float (&f)[8]) {
+    uint4 v;
+    __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&v);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+    return v;
+}
+
+// Eight E4M3FN codes of x * inv, round-to-nearest-even with saturation to +-448.
+__device__ __forceinline__ uint2 pack8_e4m3(const float (&f)[8], float inv) {
+    uint32_t w[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        uint32_t word = 0;
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            float2 p = make_float2(f[4 * h + 2 * i] * inv, f[4 * h + 2 * i + 1] * inv);
+            __nv_fp8x2_storage_t s = __nv_cvt_float2_to_fp8x2(p, __NV_SATFINITE, __NV_E4M3);
+            word |= static_cast<uint32_t>(s) << (16 * i);
+        }
+        w[h] = word;
+    }
+    return make_uint2(w[0], w[1]);
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ float half_warp_max(float v) {
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+template <int MODE, int PASSES>
+__global__ void __launch_bounds__(kThreads)
+row_norm_quant_kernel(RowArgs a) {
+    const int64_t m = blockIdx.x;
+    const int t = threadIdx.x;
+    const int lane = t & 31, warp = t >> 5;
+
+    float x[PASSES][8];
+    bool is_q[PASSES], live[PASSES];
+    int col[PASSES];  // first column (within q or within kv) of the chunk
+
+    // Issue every load of the row before touching any value.
+    uint4 raw[PASSES];
+#pragma unroll
+    for (int p = 0; p < PASSES; ++p) {
+        const int c = p * kThreads + t;
+        is_q[p] = c < a.cq;
+        live[p] = c < a.cq + a.ckv;
+        col[p] = (is_q[p] ? c : c - a.cq) * kChunk;
+        raw[p] = make_uint4(0, 0, 0, 0);
+        if (live[p]) {
+            const __nv_bfloat16* src = is_q[p] ? a.q + m * a.ldq + col[p]
+                                               : a.kv + m * a.ldkv + col[p];
+            raw[p] = __ldg(reinterpret_cast<const uint4*>(src));
+        }
+    }
+
+    if (MODE != kQuantOnly) {
+        float ssq_q = 0.f, ssq_kv = 0.f;
+#pragma unroll
+        for (int p = 0; p < PASSES; ++p) {
+            unpack8(raw[p], x[p]);
+            float s = 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) s = fmaf(x[p][i], x[p][i], s);
+            if (is_q[p]) ssq_q += s; else ssq_kv += s;   // dead chunks hold zeros
+        }
+        ssq_q = warp_sum(ssq_q);
+        ssq_kv = warp_sum(ssq_kv);
+        __shared__ float red[2][kThreads / 32];
+        if (lane == 0) { red[0][warp] = ssq_q; red[1][warp] = ssq_kv; }
+        __syncthreads();
+        ssq_q = (red[0][0] + red[0][1]) + (red[0][2] + red[0][3]);
+        ssq_kv = (red[1][0] + red[1][1]) + (red[1][2] + red[1][3]);
+        // Correctly rounded sqrt and divide (not the approximate rsqrt).
+        const float r_q = 1.0f / sqrtf(ssq_q / a.kq_f + a.eps);
+        const float r_kv = 1.0f / sqrtf(ssq_kv / a.kkv_f + a.eps);
+
+        // Gamma chunks follow the same chunk index as the row data.
+#pragma unroll
+        for (int p = 0; p < PASSES; ++p) {
+            if (!live[p]) continue;
+            const __nv_bfloat16* gsrc = is_q[p] ? a.gamma_q + col[p] : a.gamma_kv + col[p];
+            float g[8];
+            unpack8(__ldg(reinterpret_cast<const uint4*>(gsrc)), g);
+            const float r = is_q[p] ? r_q : r_kv;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) x[p][i] = (x[p][i] * r) * g[i];
+        }
+    } else {
+#pragma unroll
+        for (int p = 0; p < PASSES; ++p) unpack8(raw[p], x[p]);
+    }
+
+#pragma unroll
+    for (int p = 0; p < PASSES; ++p) {
+        if (MODE == kNormOnly) {
+            if (!live[p]) continue;
+            if (is_q[p]) {
+                *reinterpret_cast<uint4*>(a.q_bf16 + m * a.ldq_out + col[p]) = pack8_bf16(x[p]);
+            } else {
+                *reinterpret_cast<uint4*>(a.kv_out + m * a.ldkv_out + col[p]) = pack8_bf16(x[p]);
+            }
+            continue;
+        }
+        // Group amax: every aligned half-warp of this pass holds one q group,
+        // or kv / dead chunks whose result is discarded.  All lanes shuffle.
+        float amax = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(x[p][i]));
+        amax = half_warp_max(amax);
+        if (!live[p]) continue;
+        if (is_q[p]) {
+            const float inv = amax > 0.f ? kE4M3Max / amax : 0.f;
+            *reinterpret_cast<uint2*>(a.q_fp8 + m * a.ldq_out + col[p]) = pack8_e4m3(x[p], inv);
+            if ((lane & 15) == 0) {
+                const int g = col[p] / 128;
+                a.scale[m * a.scale_row_stride + g * a.scale_group_stride] = amax / kE4M3Max;
+            }
+        } else if (MODE == kFused) {
+            *reinterpret_cast<uint4*>(a.kv_out + m * a.ldkv_out + col[p]) = pack8_bf16(x[p]);
+        }
+    }
+}
+
+template <int MODE>
+static dsnq_status launch_rows(const RowArgs& a, int64_t M, cudaStream_t s) {
+    const int chunks = a.cq + a.ckv;
+    const int passes = (chunks + kThreads - 1) / kThreads;
+    dim3 grid(static_cast<unsigned>(M)), block(kThreads);
+    switch (passes) {
+        case 1: row_norm_quant_kernel<MODE, 1><<<grid, block, 0, s>>>(a); break;
+        case 2: row_norm_quant_kernel<MODE, 2><<<grid, block, 0, s>>>(a); break;
+        case 3: row_norm_quant_kernel<MODE, 3><<<grid, block, 0, s>>>(a); break;
+        case 4: row_norm_quant_kernel<MODE, 4><<<grid, block, 0, s>>>(a); break;
+        default: return DSNQ_ERR_UNSUPPORTED;
+    }
+    return launch_status();
+}
+
+// ---------------------------------------------------------------------------
+// 128x128 weight-block quantizer (load time).  One CTA per block, 256
+// threads; thread t covers row t/2 of the block, 64 columns.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256)
+weight_block_quant_kernel(int64_t N, int64_t K, const float* __restrict__ w, int64_t ldw,
+                          uint8_t* __restrict__ out, int64_t ldo,
+                          float* __restrict__ sw, int64_t ldsw) {
+    const int64_t nb = blockIdx.y, kb = blockIdx.x;
+    const int t = threadIdx.x;
+    const int64_t row = nb * 128 + t / 2;
+    const int64_t c0 = kb * 128 + (t & 1) * 64;
+    const bool live = row < N;
+    float v[64];
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        float4 f = live ? __ldg(reinterpret_cast<const float4*>(w + row * ldw + c0) + i)
+                        : make_float4(0.f, 0.f, 0.f, 0.f);
+        v[4 * i] = f.x; v[4 * i + 1] = f.y; v[4 * i + 2] = f.z; v[4 * i + 3] = f.w;
+        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(f.x), fabsf(f.y)), fmaxf(fabsf(f.z), fabsf(f.w))));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    __shared__ float red[8];
+    if ((t & 31) == 0) red[t >> 5] = amax;
+    __syncthreads();
+    amax = red[0];
+#pragma unroll
+    for (int i = 1; i < 8; ++i) amax = fmaxf(amax, red[i]);
+    const float inv = amax > 0.f ? kE4M3Max / amax : 0.f;
+    if (t == 0) sw[nb * ldsw + kb] = amax / kE4M3Max;
+    if (!live) return;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {  // 16 codes per 16-byte store
+        float f0[8], f1[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) { f0[i] = v[16 * j + i]; f1[i] = v[16 * j + 8 + i]; }
+        uint2 lo = pack8_e4m3(f0, inv), hi = pack8_e4m3(f1, inv);
+        *reinterpret_cast<uint4*>(out + row * ldo + c0 + 16 * j) = make_uint4(lo.x, lo.y, hi.x, hi.y);
+    }
+}
+
+}  // namespace dsnq
+
+using namespace dsnq;
+
+static dsnq_status check_norm_inputs(int64_t M, int64_t Kq, int64_t Kkv, const void* q, int64_t ldq,
+                                     const void* kv, int64_t ldkv, const void* gq, const void* gkv,
+                                     float eps) {
+    if (M < 0 || Kq <= 0 || Kkv <= 0) return DSNQ_ERR_INVALID_ARG;
+    if (!q || !kv || !gq || !gkv) return DSNQ_ERR_INVALID_ARG;
+    if (ldq < Kq || ldkv < Kkv) return DSNQ_ERR_INVALID_ARG;
+    if (!(eps >= 0.f) || eps != eps || eps > 3.0e38f) return DSNQ_ERR_INVALID_ARG;
+    if (Kq % 128 != 0 || Kkv % 8 != 0) return DSNQ_ERR_UNSUPPORTED;
+    if ((Kq / 8 + Kkv / 8) > 4 * kThreads) return DSNQ_ERR_UNSUPPORTED;
+    if (M > 0x7fffffffLL) return DSNQ_ERR_UNSUPPORTED;
+    if (!aligned(q, 16) || !aligned(kv, 16) || !aligned(gq, 16) || !aligned(gkv, 16))
+        return DSNQ_ERR_MISALIGNED;
+    if (ldq % 8 || ldkv % 8) return DSNQ_ERR_MISALIGNED;
+    return DSNQ_OK;
+}
+
+static void set_scale_strides(RowArgs& a, dsnq_scale_layout layout, int64_t ld) {
+    if (layout == DSNQ_SCALE_ROW_MAJOR) { a.scale_row_stride = ld; a.scale_group_stride = 1; }
+    else { a.scale_row_stride = 1; a.scale_group_stride = ld; }
+}
+
+extern "C" dsnq_status dsnq_fused_dual_rmsnorm_group_quant(
+    int64_t M, int64_t Kq, int64_t Kkv,
+    const void* q, int64_t ldq, const void* kv, int64_t ldkv,
+    const void* gamma_q, const void* gamma_kv, float eps, int32_t group,
+    void* q_fp8, int64_t ldq_out, float* q_scale, dsnq_scale_layout layout, int64_t ld_scale,
+    void* kv_out, int64_t ldkv_out, void* stream) {
+    dsnq_status st = check_norm_inputs(M, Kq, Kkv, q, ldq, kv, ldkv, gamma_q, gamma_kv, eps);
+    if (st != DSNQ_OK) return st;
+    if (layout != DSNQ_SCALE_ROW_MAJOR && layout != DSNQ_SCALE_COL_MAJOR) return DSNQ_ERR_INVALID_ARG;
+    if (group != 128) return DSNQ_ERR_UNSUPPORTED;
+    if (!q_fp8 || !q_scale || !kv_out) return DSNQ_ERR_INVALID_ARG;
+    if (ldq_out < Kq || ldkv_out < Kkv) return DSNQ_ERR_INVALID_ARG;
+    const int64_t ld = scale_ld(layout, M, Kq / 128, ld_scale);
+    if (ld < 0) return DSNQ_ERR_INVALID_ARG;
+    if (!aligned(q_fp8, 8) || ldq_out % 8 || !aligned(kv_out, 16) || ldkv_out % 8 || !aligned(q_scale, 4))
+        return DSNQ_ERR_MISALIGNED;
+    if (M == 0) return DSNQ_OK;
+    RowArgs a{};
+    a.q = static_cast<const __nv_bfloat16*>(q);
+    a.kv = static_cast<const __nv_bfloat16*>(kv);
+    a.gamma_q = static_cast<const __nv_bfloat16*>(gamma_q);
+    a.gamma_kv = static_cast<const __nv_bfloat16*>(gamma_kv);
+    a.ldq = ldq; a.ldkv = ldkv;
+    a.cq = static_cast<int>(Kq / 8); a.ckv = static_cast<int>(Kkv / 8);
+    a.kq_f = static_cast<float>(Kq); a.kkv_f = static_cast<float>(Kkv);
+    a.eps = eps;
+    a.q_fp8 = static_cast<uint8_t*>(q_fp8);
+    a.ldq_out = ldq_out;
+    a.scale = q_scale;
+    set_scale_strides(a, layout, ld);
+    a.kv_out = static_cast<__nv_bfloat16*>(kv_out);
+    a.ldkv_out = ldkv_out;
+    return launch_rows<kFused>(a, M, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" dsnq_status dsnq_dual_rmsnorm_bf16(
+    int64_t M, int64_t Kq, int64_t Kkv,
+    const void* q, int64_t ldq, const void* kv, int64_t ldkv,
+    const void* gamma_q, const void* gamma_kv, float eps,
+    void* q_out, int64_t ldq_out, void* kv_out, int64_t ldkv_out, void* stream) {
+    dsnq_status st = check_norm_inputs(M, Kq, Kkv, q, ldq, kv, ldkv, gamma_q, gamma_kv, eps);
+    if (st != DSNQ_OK) return st;
+    if (!q_out || !kv_out) return DSNQ_ERR_INVALID_ARG;
+    if (ldq_out < Kq || ldkv_out < Kkv) return DSNQ_ERR_INVALID_ARG;
+    if (!aligned(q_out, 16) || ldq_out % 8 || !aligned(kv_out, 16) || ldkv_out % 8)
+        return DSNQ_ERR_MISALIGNED;
+    if (M == 0) return DSNQ_OK;
+    RowArgs a{};
+    a.q = static_cast<const __nv_bfloat16*>(q);
+    a.kv = static_cast<const __nv_bfloat16*>(kv);
+    a.gamma_q = static_cast<const __nv_bfloat16*>(gamma_q);
+    a.gamma_kv = static_cast<const __nv_bfloat16*>(gamma_kv);
+    a.ldq = ldq; a.ldkv = ldkv;
+    a.cq = static_cast<int>(Kq / 8); a.ckv = static_cast<int>(Kkv / 8);
+    a.kq_f = static_cast<float>(Kq); a.kkv_f = static_cast<float>(Kkv);
+    a.eps = eps;
+    a.q_bf16 = static_cast<__nv_bfloat16*>(q_out);
+    a.ldq_out = ldq_out;
+    a.kv_out = static_cast<__nv_bfloat16*>(kv_out);
+    a.ldkv_out = ldkv_out;
+    return launch_rows<kNormOnly>(a, M, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" dsnq_status dsnq_group_quant_bf16(
+    int64_t M, int64_t K, const void* x, int64_t ldx, int32_t group,
+    void* x_fp8, int64_t ldx_out, float* x_scale, dsnq_scale_layout layout, int64_t ld_scale,
+    void* stream) {
+    if (M < 0 || K <= 0 || !x || !x_fp8 || !x_scale) return DSNQ_ERR_INVALID_ARG;
+    if (ldx < K || ldx_out < K) return DSNQ_ERR_INVALID_ARG;
+    if (layout != DSNQ_SCALE_ROW_MAJOR && layout != DSNQ_SCALE_COL_MAJOR) return DSNQ_ERR_INVALID_ARG;
+    if (group != 128 || K % 128 != 0 || K / 8 > 4 * kThreads) return DSNQ_ERR_UNSUPPORTED;
+    if (M > 0x7fffffffLL) return DSNQ_ERR_UNSUPPORTED;
+    const int64_t ld = scale_ld(layout, M, K / 128, ld_scale);
+    if (ld < 0) return DSNQ_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || ldx % 8 || !aligned(x_fp8, 8) || ldx_out % 8 || !aligned(x_scale, 4))
+        return DSNQ_ERR_MISALIGNED;
+    if (M == 0) return DSNQ_OK;
+    RowArgs a{};
+    a.q = static_cast<const __nv_bfloat16*>(x);
+    a.ldq = ldx;
+    a.cq = static_cast<int>(K / 8); a.ckv = 0;
+    a.q_fp8 = static_cast<uint8_t*>(x_fp8);
+    a.ldq_out = ldx_out;
+    a.scale = x_scale;
+    set_scale_strides(a, layout, ld);
+    return launch_rows<kQuantOnly>(a, M, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" dsnq_status dsnq_quantize_weight_block128(
+    int64_t N, int64_t K, const float* w, int64_t ldw, void* w_fp8, int64_t ldw_out,
+    float* w_scale, int64_t ld_wscale, void* stream) {
+    if (N < 0 || K <= 0 || !w || !w_fp8 || !w_scale) return DSNQ_ERR_INVALID_ARG;
+    if (ldw < K || ldw_out < K || ld_wscale < K / 128) return DSNQ_ERR_INVALID_ARG;
+    if (K % 128 != 0) return DSNQ_ERR_UNSUPPORTED;
+    if (!aligned(w, 16) || ldw % 4 || !aligned(w_fp8, 16) || ldw_out % 16 || !aligned(w_scale, 4))
+        return DSNQ_ERR_MISALIGNED;
+    if (N == 0) return DSNQ_OK;
+    const int64_t nb = (N + 127) / 128;
+    if (nb > 65535) return DSNQ_ERR_UNSUPPORTED;
+    dim3 grid(static_cast<unsigned>(K / 128), static_cast<unsigned>(nb));
+    weight_block_quant_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        N, K, w, ldw, static_cast<uint8_t*>(w_fp8), ldw_out, w_scale, ld_wscale);
+    return launch_status();
+}

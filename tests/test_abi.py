@@ -1,0 +1,130 @@
+"""The C ABI without a GPU: the library loads, exports every symbol that
+include/dsnq.h declares, and rejects bad arguments on the host before it
+would enqueue anything (these calls never reach the CUDA runtime)."""
+
+import ctypes as C
+import os
+import re
+
+import pytest
+
+from gemm_dsnq_dual_gb300 import _native, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dsnq.h")
+
+OK, INVALID, MISALIGNED, UNSUPPORTED = 0, 1, 2, 3
+A = 0x10000          # a 16-byte aligned fake device address (never dereferenced)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(_native.LIB_PATH):
+        build.build()
+    return _native.lib()
+
+
+def declared_functions():
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    return sorted(set(re.findall(r"\b(dsnq_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_and_binding_agree():
+    assert declared_functions() == sorted(_native.SIGNATURES)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings_and_version(lib):
+    for s, name in _native.STATUS_NAMES.items():
+        assert lib.dsnq_status_string(s).decode() == name
+    assert lib.dsnq_status_string(99).decode() == "DSNQ_ERR_UNKNOWN"
+    assert lib.dsnq_version() >= 100
+
+
+def test_quant_output_sizes(lib):
+    n, ld = C.c_int64(), C.c_int64()
+    assert lib.dsnq_quant_output_sizes(7, 1536, 128, 0, C.byref(n), C.byref(ld)) == OK
+    assert (n.value, ld.value) == (7 * 12, 12)
+    assert lib.dsnq_quant_output_sizes(7, 1536, 128, 1, C.byref(n), C.byref(ld)) == OK
+    assert (n.value, ld.value) == (7 * 12, 7)
+    assert lib.dsnq_quant_output_sizes(7, 1536, 64, 0, None, None) == UNSUPPORTED
+    assert lib.dsnq_quant_output_sizes(7, 1500, 128, 0, None, None) == UNSUPPORTED
+    assert lib.dsnq_quant_output_sizes(-1, 1536, 128, 0, None, None) == INVALID
+    assert lib.dsnq_quant_output_sizes(7, 1536, 128, 5, None, None) == INVALID
+
+
+def fused(lib, **kw):
+    a = dict(M=4, Kq=1536, Kkv=512, q=A, ldq=2112, kv=A + 3072, ldkv=2112, gq=A, gkv=A, eps=1e-6,
+             group=128, qo=A, ldqo=1536, qs=A, layout=0, lds=0, kvo=A, ldkvo=512)
+    a.update(kw)
+    return lib.dsnq_fused_dual_rmsnorm_group_quant(
+        a["M"], a["Kq"], a["Kkv"], a["q"], a["ldq"], a["kv"], a["ldkv"], a["gq"], a["gkv"], a["eps"],
+        a["group"], a["qo"], a["ldqo"], a["qs"], a["layout"], a["lds"], a["kvo"], a["ldkvo"], None)
+
+
+def test_fused_argument_checks(lib):
+    assert fused(lib, M=0) == OK                     # no rows: nothing enqueued
+    assert fused(lib, M=-1) == INVALID
+    assert fused(lib, q=None) == INVALID
+    assert fused(lib, qs=None) == INVALID
+    assert fused(lib, ldq=1000) == INVALID           # ld < width
+    assert fused(lib, layout=7) == INVALID
+    assert fused(lib, layout=1, lds=3) == INVALID    # column-major ld < M
+    assert fused(lib, layout=0, lds=11) == INVALID   # row-major ld < G
+    assert fused(lib, eps=-1.0) == INVALID
+    assert fused(lib, eps=float("nan")) == INVALID
+    assert fused(lib, group=64) == UNSUPPORTED
+    assert fused(lib, Kq=1500) == UNSUPPORTED
+    assert fused(lib, Kkv=500) == UNSUPPORTED
+    assert fused(lib, Kq=4096, Kkv=512, ldq=4608, ldkv=4608, ldqo=4096) == UNSUPPORTED  # > 4 chunks per thread
+    assert fused(lib, q=A + 8) == MISALIGNED
+    assert fused(lib, ldq=2100) == MISALIGNED
+    assert fused(lib, kvo=A + 4) == MISALIGNED
+    assert fused(lib, qo=A + 4) == MISALIGNED
+    assert fused(lib, qs=A + 2) == MISALIGNED
+
+
+def gemm(lib, **kw):
+    a = dict(M=0, N=512, K=1536, a=A, lda=1536, sa=A, lay=0, lds=0, w=A, ldw=1536, sw=A, ldsw=12,
+             o=A, ldo=512)
+    a.update(kw)
+    return lib.dsnq_block_scaled_fp8_gemm(a["M"], a["N"], a["K"], a["a"], a["lda"], a["sa"], a["lay"], a["lds"],
+                                          a["w"], a["ldw"], a["sw"], a["ldsw"], a["o"], a["ldo"], None)
+
+
+def test_gemm_argument_checks(lib):
+    assert gemm(lib) == OK                            # M == 0
+    assert gemm(lib, M=4, N=0) == OK
+    assert gemm(lib, M=-1) == INVALID
+    assert gemm(lib, a=None) == INVALID
+    assert gemm(lib, K=1000, lda=1000, ldw=1000) == UNSUPPORTED
+    assert gemm(lib, N=520, ldo=520) == UNSUPPORTED   # N % 16
+    assert gemm(lib, lda=1000) == INVALID
+    assert gemm(lib, ldsw=11) == INVALID
+    assert gemm(lib, a=A + 8) == MISALIGNED
+    assert gemm(lib, lda=1544) == MISALIGNED
+    assert gemm(lib, o=A + 2) == MISALIGNED
+    assert gemm(lib, lay=3) == INVALID
+
+
+def test_dual_and_helpers_argument_checks(lib):
+    f = lib.dsnq_block_scaled_fp8_gemm_dual
+    assert f(0, 1536, A, 1536, A, 0, 0, 512, A, 1536, A, 12, A, 512, 256, A, 1536, A, 12, A, 256, None) == OK
+    assert f(4, 1536, A, 1536, A, 0, 0, 512, A, 1536, A, 12, A, 512, 256, A + 1, 1536, A, 12, A, 256, None) == MISALIGNED
+    assert f(4, 1536, A, 1536, A, 0, 0, 0, None, 0, None, 0, None, 0, 0, None, 0, None, 0, None, 0, None) == OK
+    assert lib.dsnq_group_quant_bf16(0, 1536, A, 1536, 128, A, 1536, A, 0, 0, None) == OK
+    assert lib.dsnq_group_quant_bf16(4, 1536, A, 1536, 32, A, 1536, A, 0, 0, None) == UNSUPPORTED
+    assert lib.dsnq_quantize_weight_block128(0, 1536, A, 1536, A, 1536, A, 12, None) == OK
+    assert lib.dsnq_quantize_weight_block128(4, 1500, A, 1500, A, 1536, A, 12, None) == UNSUPPORTED
+    assert lib.dsnq_dual_rmsnorm_bf16(0, 1536, 512, A, 1536, A, 512, A, A, 1e-6, A, 1536, A, 512, None) == OK
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    monkeypatch.setattr(_native, "_lib", None)
+    monkeypatch.setattr(_native, "LIB_PATH", str(tmp_path / "libdsnq.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        _native.lib()
