@@ -31,7 +31,7 @@ __all__ = [
     "ROW_MAJOR", "COL_MAJOR", "DsnqError",
     "fused_dual_rmsnorm_group_quant", "dual_rmsnorm_bf16", "group_quant_bf16",
     "quantize_weight_block128", "block_scaled_fp8_gemm", "block_scaled_fp8_gemm_dual",
-    "quant_output_sizes", "debug_status", "debug_set", "scale_layout_of", "empty_scales",
+    "quant_output_sizes", "debug_status", "debug_set", "scale_layout_of", "scale_ld_for", "empty_scales",
 ]
 
 
@@ -72,6 +72,19 @@ def empty_scales(M: int, G: int, layout, device) -> torch.Tensor:
     return torch.empty(G, M, dtype=torch.float32, device=device).t()
 
 
+def scale_ld_for(scale: torch.Tensor, layout) -> int:
+    """Leading dimension of a logical [M, G] scale tensor read in `layout`;
+    raises if its memory does not have that layout."""
+    M, G = scale.shape
+    if _layout(layout) == ROW_MAJOR:
+        if G > 1 and scale.stride(1) != 1:
+            raise ValueError("scale tensor is not row-major")
+        return scale.stride(0) if M > 1 else G
+    if M > 1 and scale.stride(0) != 1:
+        raise ValueError("scale tensor is not column-major")
+    return scale.stride(1) if G > 1 else M
+
+
 def scale_layout_of(scale: torch.Tensor):
     """(layout, ld) of a logical [M, G] scale tensor."""
     M, G = scale.shape
@@ -98,9 +111,7 @@ def fused_dual_rmsnorm_group_quant(q, kv, gamma_q, gamma_kv, eps: float = 1e-6, 
         q_scale = empty_scales(M, Kq // group, lay, dev)
     if kv_out is None:
         kv_out = torch.empty(M, Kkv, dtype=torch.bfloat16, device=dev)
-    lay2, ld = scale_layout_of(q_scale)
-    if M > 1 and Kq // group > 1 and lay2 != lay:
-        raise ValueError("q_scale memory layout does not match scale_layout")
+    ld = scale_ld_for(q_scale, lay)
     check(lib().dsnq_fused_dual_rmsnorm_group_quant(
         M, Kq, Kkv, q.data_ptr(), _row_view_ok(q, "q"), kv.data_ptr(), _row_view_ok(kv, "kv"),
         gamma_q.data_ptr(), gamma_kv.data_ptr(), float(eps), group,
@@ -134,7 +145,7 @@ def group_quant_bf16(x, group: int = GROUP, scale_layout=ROW_MAJOR, x_out=None, 
         x_out = torch.empty(M, K, dtype=torch.float8_e4m3fn, device=x.device)
     if x_scale is None:
         x_scale = empty_scales(M, K // group, lay, x.device)
-    _, ld = scale_layout_of(x_scale)
+    ld = scale_ld_for(x_scale, lay)
     check(lib().dsnq_group_quant_bf16(
         M, K, x.data_ptr(), _row_view_ok(x, "x"), group, x_out.data_ptr(), _row_view_ok(x_out, "x_out"),
         x_scale.data_ptr(), lay, ld, _stream(stream)), "dsnq_group_quant_bf16")

@@ -50,8 +50,6 @@ namespace gemm {
 constexpr int kBK = 128;            // K bytes per stage = one scale block
 constexpr int kUmmaK = 32;          // K per tcgen05.mma kind::f8f6f4
 constexpr int kPRows = 128;         // MMA M
-constexpr int kEpiWarps = 8;
-constexpr int kThreads = (2 + kEpiWarps) * 32;
 constexpr uint32_t kStatusTimeout = 1u;
 
 __device__ unsigned int g_status;   // device status word (bit 0: a wait timed out)
@@ -71,6 +69,7 @@ struct Params {
     int64_t as_rs, as_gs;          // sa(m, g) = a_scale[m * as_rs + g * as_gs]
     int tiles_m;                   // tiles along the activation rows
     int tiles0;                    // tiles of problem 0
+    int total_tiles;               // tiles of both problems
     Problem prob[2];
     uint64_t timeout_ns;
     uint32_t inject;
@@ -242,70 +241,83 @@ __device__ __forceinline__ void named_bar_sync(int id, int count) {
 
 // ------------------------------------------------------------------- kernel
 
-template <int BN, bool SWAP, int STAGES>
+// Compile-time shape of one kernel variant.
+//   BN        MMA N (rows of the Q operand per tile)
+//   SWAP      false: P = activations, Q = weights; true: P = weights, Q = activations
+//   STAGES    depth of the shared-memory ring (one 128-wide K block per stage)
+//   NBUF      TMEM partial-sum buffers (the MMA may run NBUF-1 K blocks ahead)
+//   EPI_WARPS promotion warps (a multiple of 4: one per TMEM lane quarter and slice)
+template <int BN, bool SWAP, int STAGES, int NBUF, int EPI_WARPS>
 struct Cfg {
     static constexpr int kPBytes = kPRows * kBK;       // 16 KB
     static constexpr int kQBytes = BN * kBK;
     static constexpr int kStageBytes = kPBytes + kQBytes;
-    static constexpr int kTmemCols = (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128
-                                     : (2 * BN <= 256) ? 256 : 512;
-    static constexpr int kHalf = BN / 2;                // columns per epilogue thread
-    static constexpr int kLd = kHalf >= 32 ? 32 : kHalf;  // columns per tcgen05.ld
+    static constexpr int kTmemNeed = NBUF * BN;
+    static constexpr int kTmemCols = kTmemNeed <= 32 ? 32 : kTmemNeed <= 64 ? 64 : kTmemNeed <= 128 ? 128
+                                     : kTmemNeed <= 256 ? 256 : 512;
+    static constexpr int kSlices = EPI_WARPS / 4;       // column slices per lane quarter
+    static constexpr int kCols = BN / kSlices;          // tile columns per promotion thread
+    static constexpr int kLd = kCols >= 64 ? 32 : (kCols >= 16 ? 16 : kCols);  // columns per tcgen05.ld
+    static constexpr int kThreads = (2 + EPI_WARPS) * 32;
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M=128 is 16..256 step 16");
-    static_assert(kHalf % 8 == 0, "epilogue reads TMEM 8 columns at a time at least");
-    // Non-swap: each epilogue half must stay inside one 128-feature scale block.
-    static_assert(SWAP || BN == 128 || BN == 256, "non-swap tiles are 128 or 256 features wide");
+    static_assert(kTmemNeed <= 512, "TMEM holds 512 fp32 columns");
+    static_assert(EPI_WARPS % 4 == 0 && BN % kSlices == 0, "promotion warps tile the accumulator");
+    static_assert(kCols % 8 == 0 && kCols % kLd == 0, "TMEM is read 8 columns at a time at least");
+    // Non-swap: a thread's columns must share one 128-feature weight-scale block.
+    static_assert(SWAP || (kPRows % kCols == 0), "non-swap slices stay inside a scale block");
 };
 
-template <int BN, bool SWAP, int STAGES>
-__global__ void __launch_bounds__(kThreads, 1)
+// Tile t of the concatenated tile space -> (problem, first activation row, first feature).
+// Activation tiles vary fastest, so CTAs running together share weight tiles in L2.
+template <int BN, bool SWAP>
+__device__ __forceinline__ void tile_coords(const Params& p, int t, int& pi, int& m0, int& n0) {
+    pi = t < p.tiles0 ? 0 : 1;
+    if (pi) t -= p.tiles0;
+    const int tm = t % p.tiles_m, tn = t / p.tiles_m;
+    m0 = SWAP ? tm * BN : tm * kPRows;
+    n0 = SWAP ? tn * kPRows : tn * BN;
+}
+
+template <int BN, bool SWAP, int STAGES, int NBUF, int EPI_WARPS>
+__global__ void __launch_bounds__(Cfg<BN, SWAP, STAGES, NBUF, EPI_WARPS>::kThreads, 1)
 block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                          const __grid_constant__ CUtensorMap map_w0,
                          const __grid_constant__ CUtensorMap map_w1,
                          const Params p) {
-    using C = Cfg<BN, SWAP, STAGES>;
+    using C = Cfg<BN, SWAP, STAGES, NBUF, EPI_WARPS>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 1024-byte alignment for the 128-byte-swizzled tiles.
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* tiles = smem;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * C::kStageBytes);
-    uint64_t* full = bars;                 // [STAGES]  TMA -> MMA
-    uint64_t* empty = bars + STAGES;       // [STAGES]  MMA -> TMA
-    uint64_t* tfull = bars + 2 * STAGES;   // [2]       MMA -> promotion
-    uint64_t* tempty = tfull + 2;          // [2]       promotion -> MMA
-    uint64_t* drain = tempty + 2;          // [1]       abort drain of MMAs
+    uint64_t* full = bars;                    // [STAGES] TMA -> MMA
+    uint64_t* empty = bars + STAGES;          // [STAGES] MMA -> TMA
+    uint64_t* tfull = bars + 2 * STAGES;      // [NBUF]   MMA -> promotion
+    uint64_t* tempty = tfull + NBUF;          // [NBUF]   promotion -> MMA
+    uint64_t* drain = tempty + NBUF;          // [1]      abort drain of MMAs
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
     float* sq = reinterpret_cast<float*>(tmem_holder + 4);  // swap: [KB][BN] combined scales
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-
-    // ---- tile of this CTA
-    int t = blockIdx.x;
-    const int pi = t < p.tiles0 ? 0 : 1;
-    if (pi) t -= p.tiles0;
-    const Problem pr = pi ? p.prob[1] : p.prob[0];
-    const CUtensorMap* map_w = pi ? &map_w1 : &map_w0;
-    const int tm = t % p.tiles_m, tn = t / p.tiles_m;
-    // Activation rows [m0, m0 + rowsA), features [n0, n0 + rowsW).
-    const int m0 = SWAP ? tm * BN : tm * kPRows;
-    const int n0 = SWAP ? tn * kPRows : tn * BN;
+    const int total = p.total_tiles;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(smem_u32(&full[s]), 1);
             mbar_init(smem_u32(&empty[s]), 1);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < NBUF; ++b) {
             mbar_init(smem_u32(&tfull[b]), 1);
-            mbar_init(smem_u32(&tempty[b]), kEpiWarps);
+            mbar_init(smem_u32(&tempty[b]), EPI_WARPS);
         }
         mbar_init(smem_u32(drain), 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         tma_prefetch_desc(&map_a);
-        tma_prefetch_desc(map_w);
+        tma_prefetch_desc(&map_w0);
+        tma_prefetch_desc(&map_w1);
     }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_holder)),
@@ -320,32 +332,38 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
     const uint64_t tmo = p.timeout_ns;
 
     if (warp == 0) {
-        // ------------------------------------------------ TMA producer
+        // ------------------------------------------------ TMA producer (one lane)
         if (lane == 0) {
-            const CUtensorMap* map_p = SWAP ? map_w : &map_a;
-            const CUtensorMap* map_q = SWAP ? &map_a : map_w;
-            const int p_row = SWAP ? n0 : m0;
-            const int q_row = SWAP ? m0 : n0;
-            int issued = 0;  // K blocks whose loads were issued
+            uint32_t g = 0;  // K blocks of this CTA so far, across tiles
             bool ok = true;
-            for (int kb = 0; kb < p.KB; ++kb) {
-                const int s = kb % STAGES;
-                const uint32_t ph = (kb / STAGES) & 1;
-                if (!wait_bounded(smem_u32(&empty[s]), ph ^ 1, abort_flag, tmo)) { ok = false; break; }
-                if ((p.inject & 1u) && kb == 0) continue;   // test hook: never arrive on full[0]
-                const uint32_t fb = smem_u32(&full[s]);
-                mbar_arrive_expect_tx(fb, C::kStageBytes);
-                uint8_t* st = tiles + s * C::kStageBytes;
-                tma_load_2d(smem_u32(st), map_p, fb, kb * kBK, p_row);
-                tma_load_2d(smem_u32(st + C::kPBytes), map_q, fb, kb * kBK, q_row);
-                issued = kb + 1;
+            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+                int pi, m0, n0;
+                tile_coords<BN, SWAP>(p, t, pi, m0, n0);
+                const CUtensorMap* map_w = pi ? &map_w1 : &map_w0;
+                const CUtensorMap* map_p = SWAP ? map_w : &map_a;
+                const CUtensorMap* map_q = SWAP ? &map_a : map_w;
+                const int p_row = SWAP ? n0 : m0;
+                const int q_row = SWAP ? m0 : n0;
+                for (int kb = 0; kb < p.KB; ++kb, ++g) {
+                    const int s = g % STAGES;
+                    if (!wait_bounded(smem_u32(&empty[s]), ((g / STAGES) & 1) ^ 1, abort_flag, tmo)) {
+                        ok = false;
+                        break;
+                    }
+                    if ((p.inject & 1u) && g == 0) continue;   // test hook: never arrive on full[0]
+                    const uint32_t fb = smem_u32(&full[s]);
+                    mbar_arrive_expect_tx(fb, C::kStageBytes);
+                    uint8_t* st = tiles + s * C::kStageBytes;
+                    tma_load_2d(smem_u32(st), map_p, fb, kb * kBK, p_row);
+                    tma_load_2d(smem_u32(st + C::kPBytes), map_q, fb, kb * kBK, q_row);
+                }
             }
             if (!ok || *abort_flag) {
                 // Let the copies already issued land before the CTA exits.
-                const int first = issued > STAGES ? issued - STAGES : 0;
-                for (int kb = first; kb < issued; ++kb) {
-                    if ((p.inject & 1u) && kb == 0) continue;
-                    wait_drain(smem_u32(&full[kb % STAGES]), (kb / STAGES) & 1, tmo);
+                const uint32_t first = g > STAGES ? g - STAGES : 0;
+                for (uint32_t j = first; j < g; ++j) {
+                    if ((p.inject & 1u) && j == 0) continue;
+                    wait_drain(smem_u32(&full[j % STAGES]), (j / STAGES) & 1, tmo);
                 }
             }
         }
@@ -353,100 +371,116 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
         // ------------------------------------------------ MMA issuer (one lane)
         constexpr uint32_t idesc = idesc_e4m3(BN);
         if (lane == 0) {
-            int issued = 0;
-            for (int kb = 0; kb < p.KB; ++kb) {
-                const int s = kb % STAGES;
-                const int b = kb & 1;
-                if (!wait_bounded(smem_u32(&full[s]), (kb / STAGES) & 1, abort_flag, tmo)) break;
-                if (!wait_bounded(smem_u32(&tempty[b]), ((kb >> 1) & 1) ^ 1, abort_flag, tmo)) break;
-                tc_fence_after();
-                const uint32_t pa = smem_u32(tiles + s * C::kStageBytes);
-                const uint32_t qa = pa + C::kPBytes;
-                const uint32_t d = tmem_base + static_cast<uint32_t>(b * BN);
+            uint32_t g = 0;
+            bool ok = true, any = false;
+            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+                for (int kb = 0; kb < p.KB; ++kb, ++g) {
+                    const int s = g % STAGES;
+                    const int b = g % NBUF;
+                    if (!wait_bounded(smem_u32(&full[s]), (g / STAGES) & 1, abort_flag, tmo) ||
+                        !wait_bounded(smem_u32(&tempty[b]), ((g / NBUF) & 1) ^ 1, abort_flag, tmo)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t pa = smem_u32(tiles + s * C::kStageBytes);
+                    const uint32_t qa = pa + C::kPBytes;
+                    const uint32_t d = tmem_base + static_cast<uint32_t>(b * BN);
 #pragma unroll
-                for (int k = 0; k < kBK / kUmmaK; ++k) {
-                    tc_mma_f8(d, smem_desc_k_sw128(pa + k * kUmmaK), smem_desc_k_sw128(qa + k * kUmmaK), idesc,
-                              k > 0 ? 1u : 0u);
+                    for (int k = 0; k < kBK / kUmmaK; ++k) {
+                        tc_mma_f8(d, smem_desc_k_sw128(pa + k * kUmmaK), smem_desc_k_sw128(qa + k * kUmmaK),
+                                  idesc, k > 0 ? 1u : 0u);
+                    }
+                    tc_commit(smem_u32(&empty[s]));    // stage free once these MMAs have read it
+                    tc_commit(smem_u32(&tfull[b]));    // partial sum ready
+                    any = true;
                 }
-                tc_commit(smem_u32(&empty[s]));
-                tc_commit(smem_u32(&tfull[b]));
-                issued = kb + 1;
             }
-            if (*abort_flag && issued > 0) {
-                tc_commit(smem_u32(drain));       // completes once every MMA above has
+            if (*abort_flag && any) {
+                tc_commit(smem_u32(drain));            // completes once every MMA above has
                 wait_drain(smem_u32(drain), 0, tmo);
             }
         }
         __syncwarp();
     } else {
         // ------------------------------------------------ promotion + store
-        const int ew = warp - 2;                 // 0..7
-        const int quarter = warp & 3;            // TMEM lanes 32*quarter..+31
-        const int half = ew >> 2;                // column half of the tile
+        const int ew = warp - 2;                 // 0 .. EPI_WARPS-1
+        const int quarter = warp & 3;            // TMEM lanes 32*quarter .. +31
+        const int slice = ew >> 2;               // column slice of the tile
         const int row = quarter * 32 + lane;     // P row (TMEM lane)
-        const int col0 = half * C::kHalf;
-
-        if (SWAP) {
-            // Combined scale sa(m0+j, kb) * sw[n0/128, kb] for every token j.
-            const int nb = n0 / kPRows;
-            for (int i = threadIdx.x - 64; i < p.KB * BN; i += kEpiWarps * 32) {
-                const int kb = i / BN, j = i % BN;
-                const int m = m0 + j;
-                float v = 0.f;
-                if (m < p.M) v = p.a_scale[m * p.as_rs + kb * p.as_gs] * pr.w_scale[nb * pr.ld_ws + kb];
-                sq[i] = v;
-            }
-            named_bar_sync(1, kEpiWarps * 32);
-        }
-
-        float acc[C::kHalf];
-#pragma unroll
-        for (int j = 0; j < C::kHalf; ++j) acc[j] = 0.f;
-
-        const int m_row = m0 + row;                           // non-swap: token of this thread
-        const int nb_ns = (n0 + col0) / kPRows;               // non-swap: scale block of the half
+        const int col0 = slice * C::kCols;
+        uint32_t g = 0;
         bool ok = true;
-        for (int kb = 0; kb < p.KB; ++kb) {
-            const int b = kb & 1;
-            float srow = 0.f;
-            if (!SWAP) {
-                if (m_row < p.M)
-                    srow = p.a_scale[m_row * p.as_rs + kb * p.as_gs] * pr.w_scale[nb_ns * pr.ld_ws + kb];
+        for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+            int pi, m0, n0;
+            tile_coords<BN, SWAP>(p, t, pi, m0, n0);
+            const Problem pr = pi ? p.prob[1] : p.prob[0];
+            if (SWAP) {
+                // Combined scale sa(m0+j, kb) * sw[n0/128, kb] for every token j of the tile.
+                named_bar_sync(1, EPI_WARPS * 32);     // previous tile's readers are done
+                const int nb = n0 / kPRows;
+                for (int i = threadIdx.x - 64; i < p.KB * BN; i += EPI_WARPS * 32) {
+                    const int kb = i / BN, j = i % BN;
+                    const int m = m0 + j;
+                    float v = 0.f;
+                    if (m < p.M) v = p.a_scale[m * p.as_rs + kb * p.as_gs] * pr.w_scale[nb * pr.ld_ws + kb];
+                    sq[i] = v;
+                }
+                named_bar_sync(1, EPI_WARPS * 32);
             }
-            // Every lane polls (each acquires the phase); the outcome is made
-            // warp-uniform before the warp-collective TMEM loads.
-            const bool got = wait_bounded(smem_u32(&tfull[b]), (kb >> 1) & 1, abort_flag, tmo);
-            if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
-            tc_fence_after();
-            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
-                                   static_cast<uint32_t>(b * BN + col0);
+
+            float acc[C::kCols];
 #pragma unroll
-            for (int c = 0; c < C::kHalf; c += C::kLd) {
-                uint32_t r[C::kLd];
-                tmem_ld<C::kLd>(taddr + c, r);
-                tmem_ld_wait();
+            for (int j = 0; j < C::kCols; ++j) acc[j] = 0.f;
+            const int m_row = m0 + row;                       // non-swap: token of this thread
+            const int nb_ns = (n0 + col0) / kPRows;           // non-swap: scale block of the slice
+
+            for (int kb = 0; kb < p.KB; ++kb, ++g) {
+                const int b = g % NBUF;
+                float srow = 0.f;
+                if (!SWAP && m_row < p.M)
+                    srow = p.a_scale[m_row * p.as_rs + kb * p.as_gs] * pr.w_scale[nb_ns * pr.ld_ws + kb];
+                // Every lane polls (each acquires the phase); the outcome is made
+                // warp-uniform before the warp-collective TMEM loads.
+                const bool got = wait_bounded(smem_u32(&tfull[b]), (g / NBUF) & 1, abort_flag, tmo);
+                if (!__all_sync(0xffffffffu, got)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                       static_cast<uint32_t>(b * BN + col0);
 #pragma unroll
-                for (int j = 0; j < C::kLd; ++j) {
-                    const float s = SWAP ? sq[kb * BN + col0 + c + j] : srow;
-                    acc[c + j] = fmaf(__uint_as_float(r[j]), s, acc[c + j]);
+                for (int c = 0; c < C::kCols; c += C::kLd) {
+                    uint32_t r[C::kLd];
+                    tmem_ld<C::kLd>(taddr + c, r);
+                    tmem_ld_wait();
+                    if (c + C::kLd == C::kCols) {
+                        // Last read of this buffer: hand it back to the MMA warp.
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(smem_u32(&tempty[b]));
+                    }
+#pragma unroll
+                    for (int j = 0; j < C::kLd; ++j) {
+                        const float sc = SWAP ? sq[kb * BN + col0 + c + j] : srow;
+                        acc[c + j] = fmaf(__uint_as_float(r[j]), sc, acc[c + j]);
+                    }
                 }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&tempty[b]));
-        }
+            if (!ok) break;
 
-        if (ok) {
             if (!SWAP) {
                 if (m_row < p.M) {
                     __nv_bfloat16* dst = pr.out + static_cast<int64_t>(m_row) * pr.ldo + n0 + col0;
 #pragma unroll
-                    for (int c = 0; c < C::kHalf; c += 8) {
+                    for (int c = 0; c < C::kCols; c += 8) {
                         if (n0 + col0 + c < pr.N) {
                             uint4 v;
                             __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&v);
 #pragma unroll
-                            for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(acc[c + 2 * i], acc[c + 2 * i + 1]);
+                            for (int i = 0; i < 4; ++i)
+                                h[i] = __floats2bfloat162_rn(acc[c + 2 * i], acc[c + 2 * i + 1]);
                             *reinterpret_cast<uint4*>(dst + c) = v;
                         }
                     }
@@ -455,7 +489,7 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                 const int n = n0 + row;
                 if (n < pr.N) {
 #pragma unroll
-                    for (int j = 0; j < C::kHalf; ++j) {
+                    for (int j = 0; j < C::kCols; ++j) {
                         const int m = m0 + col0 + j;
                         if (m < p.M) pr.out[static_cast<int64_t>(m) * pr.ldo + n] = __float2bfloat16_rn(acc[j]);
                     }
@@ -473,10 +507,10 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
     }
 }
 
-template <int BN, bool SWAP, int STAGES>
+template <int BN, bool SWAP, int STAGES, int NBUF, int EPI_WARPS>
 constexpr size_t smem_bytes(int KB) {
-    using C = Cfg<BN, SWAP, STAGES>;
-    return 1024 /* alignment slack */ + STAGES * C::kStageBytes + (2 * STAGES + 5) * 8 + 16 +
+    using C = Cfg<BN, SWAP, STAGES, NBUF, EPI_WARPS>;
+    return 1024 /* alignment slack */ + STAGES * C::kStageBytes + (2 * STAGES + 2 * NBUF + 1) * 8 + 16 +
            (SWAP ? static_cast<size_t>(KB) * BN * 4 : 0);
 }
 
@@ -544,29 +578,36 @@ dsnq_status check_consumer(const Consumer& c, int64_t K) {
     return DSNQ_OK;
 }
 
-template <int BN, bool SWAP, int STAGES>
-dsnq_status launch(const gemm::Params& prm, const CUtensorMap& ma, const CUtensorMap& mw0, const CUtensorMap& mw1,
-                   int total_tiles, cudaStream_t stream) {
-    auto kern = gemm::block_scaled_gemm_kernel<BN, SWAP, STAGES>;
-    const size_t smem = gemm::smem_bytes<BN, SWAP, STAGES>(prm.KB);
+template <int BN, bool SWAP, int STAGES, int NBUF, int EPI_WARPS>
+dsnq_status launch(gemm::Params& prm, const CUtensorMap& ma, const CUtensorMap& mw0, const CUtensorMap& mw1,
+                   cudaStream_t stream) {
+    using C = gemm::Cfg<BN, SWAP, STAGES, NBUF, EPI_WARPS>;
+    auto kern = gemm::block_scaled_gemm_kernel<BN, SWAP, STAGES, NBUF, EPI_WARPS>;
+    const size_t smem = gemm::smem_bytes<BN, SWAP, STAGES, NBUF, EPI_WARPS>(prm.KB);
     if (smem > 227 * 1024) return DSNQ_ERR_UNSUPPORTED;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
         cudaSuccess) {
         cudaGetLastError();
         return DSNQ_ERR_CUDA;
     }
-    kern<<<total_tiles, gemm::kThreads, smem, stream>>>(ma, mw0, mw1, prm);
+    // Persistent: one CTA per SM (the shared-memory ring allows one), each
+    // walking the tile space with a stride of the grid size.
+    const int sms = device_sm_count();
+    const int grid = prm.total_tiles < sms ? prm.total_tiles : (sms > 0 ? sms : prm.total_tiles);
+    kern<<<grid, C::kThreads, smem, stream>>>(ma, mw0, mw1, prm);
     return launch_status();
 }
 
 dsnq_status run_gemm(int64_t M, int64_t K, const void* a, int64_t lda, const float* as,
                      dsnq_scale_layout layout, int64_t ld_as, const Consumer& c0, const Consumer& c1,
                      void* stream) {
-    if (M < 0 || K <= 0 || !a || !as) return DSNQ_ERR_INVALID_ARG;
+    if (M < 0 || K <= 0 || c0.N < 0 || c1.N < 0) return DSNQ_ERR_INVALID_ARG;
     if (layout != DSNQ_SCALE_ROW_MAJOR && layout != DSNQ_SCALE_COL_MAJOR) return DSNQ_ERR_INVALID_ARG;
-    if (lda < K) return DSNQ_ERR_INVALID_ARG;
     if (K % 128 != 0) return DSNQ_ERR_UNSUPPORTED;
     if (M > 0x7fffffffLL || K > (1LL << 20)) return DSNQ_ERR_UNSUPPORTED;
+    if (M == 0) return DSNQ_OK;          // empty activations may come with NULL pointers
+    if (!a || !as) return DSNQ_ERR_INVALID_ARG;
+    if (lda < K) return DSNQ_ERR_INVALID_ARG;
     const int64_t KB = K / 128;
     const int64_t ld = scale_ld(layout, M, KB, ld_as);
     if (ld < 0) return DSNQ_ERR_INVALID_ARG;
@@ -575,8 +616,10 @@ dsnq_status run_gemm(int64_t M, int64_t K, const void* a, int64_t lda, const flo
     if (st != DSNQ_OK) return st;
     st = check_consumer(c1, K);
     if (st != DSNQ_OK) return st;
-    if (M == 0 || (c0.N == 0 && c1.N == 0)) return DSNQ_OK;
+    if (c0.N == 0 && c1.N == 0) return DSNQ_OK;
 
+    // Decode batches (M <= 64): swap-AB, the tokens are the MMA's N.
+    // Otherwise 128x128 tiles with four TMEM partial buffers.
     const bool swap = M <= 64;
     const int bn = swap ? (M <= 16 ? 16 : M <= 32 ? 32 : 64) : 128;
     const int a_box = swap ? bn : gemm::kPRows;
@@ -616,17 +659,17 @@ dsnq_status run_gemm(int64_t M, int64_t K, const void* a, int64_t lda, const flo
     }
     if (np == 1) mw[1] = mw[0];
     if (total > 0x7fffffffLL) return DSNQ_ERR_UNSUPPORTED;
+    prm.total_tiles = static_cast<int>(total);
     const uint64_t tmo = g_timeout_ns.load();
     prm.timeout_ns = tmo ? tmo : kDefaultTimeoutNs;
     prm.inject = g_inject.load();
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const int tt = static_cast<int>(total);
-    if (!swap) return launch<128, false, 4>(prm, ma, mw[0], mw[1], tt, s);
     switch (bn) {
-        case 16: return launch<16, true, 8>(prm, ma, mw[0], mw[1], tt, s);
-        case 32: return launch<32, true, 8>(prm, ma, mw[0], mw[1], tt, s);
-        default: return launch<64, true, 8>(prm, ma, mw[0], mw[1], tt, s);
+        case 16: return launch<16, true, 8, 4, 8>(prm, ma, mw[0], mw[1], s);
+        case 32: return launch<32, true, 8, 4, 8>(prm, ma, mw[0], mw[1], s);
+        case 64: return launch<64, true, 8, 4, 8>(prm, ma, mw[0], mw[1], s);
+        default: return launch<128, false, 6, 4, 8>(prm, ma, mw[0], mw[1], s);
     }
 }
 
@@ -640,7 +683,6 @@ extern "C" dsnq_status dsnq_block_scaled_fp8_gemm(int64_t M, int64_t N, int64_t 
                                                  int64_t ld_ascale, const void* w_fp8, int64_t ldw,
                                                  const float* w_scale, int64_t ld_wscale, void* out_bf16,
                                                  int64_t ldo, void* stream) {
-    if (N <= 0) return N == 0 ? DSNQ_OK : DSNQ_ERR_INVALID_ARG;
     Consumer c0{N, w_fp8, ldw, w_scale, ld_wscale, out_bf16, ldo};
     Consumer c1{0, nullptr, 0, nullptr, 0, nullptr, 0};
     return run_gemm(M, K, a_fp8, lda, a_scale, a_scale_layout, ld_ascale, c0, c1, stream);

@@ -6,20 +6,24 @@
 // with fp32 scales in the same pass, reading the fp32 values (one rounding);
 // kv stays bf16.  Scale layout switch: sglang PR #27289 ("transpose_scale").
 //
-// Kernel shape (one CTA = one warp-group = one token row):
+// Kernel shape (one CTA = one warp-group; rows are processed in a
+// grid-stride loop so the per-thread set-up is paid once per CTA):
 //   * a row is cut into 16-byte chunks of 8 bf16; chunk c < Kq/8 is q, the
 //     rest is kv.  Thread t owns chunks t, t+128, ... (PASSES of them), so a
 //     DSv4 row (192 q chunks + 64 kv chunks) is exactly two 16-byte loads per
 //     thread, coalesced, from strided split views as well as contiguous rows;
+//   * the thread's gamma chunks are loaded once, as fp32, and the next row's
+//     chunks are loaded while the current row is reduced and stored;
 //   * the two sums of squares are reduced with warp shuffles and one
-//     cross-warp step through shared memory;
+//     cross-warp step through shared memory (double-buffered by row parity,
+//     so one barrier per row suffices);
 //   * Kq is a multiple of 128, so in every pass each aligned half-warp holds
 //     exactly one 128-column q group (or kv, or nothing): the group amax is a
 //     4-step 16-lane shuffle, and lane 0 of the half-warp stores the scale;
+//   * elementwise fp32 work uses the packed f32x2 instructions of sm_100+;
 //   * codes are packed 8 per thread and stored as one 8-byte word, kv as one
 //     16-byte word.
-// The whole row stays in registers between the reductions and the stores, so
-// each input byte is read once and each output byte written once.
+// Each input byte is read once and each output byte written once.
 
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
@@ -31,6 +35,9 @@ namespace dsnq {
 
 constexpr int kThreads = 128;       // one warp-group per row
 constexpr int kChunk = 8;           // bf16 per 16-byte chunk
+// CTAs per SM the register budget is sized for (64 registers per thread up
+// to two chunks per thread, 128 beyond).
+__host__ __device__ constexpr int min_blocks_per_sm(int passes) { return passes <= 2 ? 8 : 4; }
 constexpr float kE4M3Max = 448.0f;  // largest finite E4M3FN value
 
 enum Mode : int {
@@ -45,6 +52,7 @@ struct RowArgs {
     const __nv_bfloat16* gamma_q;
     const __nv_bfloat16* gamma_kv;
     int64_t ldq, ldkv;
+    int64_t M;
     int cq, ckv;           // chunk counts Kq/8, Kkv/8
     float kq_f, kkv_f;     // Kq and Kkv as floats (divisors of the mean)
     float eps;
@@ -57,34 +65,57 @@ struct RowArgs {
     int64_t ldkv_out;
 };
 
-__device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
-    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        float2 t = __bfloat1622float2(h[i]);
-        f[2 * i] = t.x;
-        f[2 * i + 1] = t.y;
-    }
+// ---- packed fp32 pairs (f32x2 instructions, sm_100+)
+__device__ __forceinline__ uint64_t as_u64(float2 v) {
+    return (static_cast<uint64_t>(__float_as_uint(v.y)) << 32) | __float_as_uint(v.x);
+}
+__device__ __forceinline__ float2 as_f2(uint64_t v) {
+    return make_float2(__uint_as_float(static_cast<uint32_t>(v)), __uint_as_float(static_cast<uint32_t>(v >> 32)));
+}
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(as_u64(a)), "l"(as_u64(b)));
+    return as_f2(d);
+}
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(as_u64(a)), "l"(as_u64(b)), "l"(as_u64(c)));
+    return as_f2(d);
 }
 
-__device__ __forceinline__ uint4 pack8_bf16(const float (&f)[8]) {
+// Eight bf16 of a 16-byte chunk as four fp32 pairs (exact: bf16 is the top
+// half of an fp32).
+__device__ __forceinline__ void unpack8(const uint4& v, float2 (&f)[4]) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) f[i] = make_float2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xFFFF0000u));
+}
+
+__device__ __forceinline__ uint4 pack8_bf16(const float2 (&f)[4]) {
     uint4 v;
     __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&v);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+    for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(f[i].x, f[i].y);
     return v;
 }
 
-// Eight E4M3FN codes of x * inv, round-to-nearest-even with saturation to +-448.
-__device__ __forceinline__ uint2 pack8_e4m3(const float (&f)[8], float inv) {
+// Quotient of the quantize step: the IEEE fp32 division x / scale, or a
+// signed zero for an all-zero group (scale == 0).
+__device__ __forceinline__ float quant_quotient(float x, float scale) {
+    return scale > 0.f ? __fdiv_rn(x, scale) : x * 0.f;
+}
+
+// Eight E4M3FN codes of x / scale, round-to-nearest-even with saturation to +-448.
+__device__ __forceinline__ uint2 pack8_e4m3(const float2 (&f)[4], float scale) {
     uint32_t w[2];
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
         uint32_t word = 0;
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
-            float2 p = make_float2(f[4 * h + 2 * i] * inv, f[4 * h + 2 * i + 1] * inv);
-            __nv_fp8x2_storage_t s = __nv_cvt_float2_to_fp8x2(p, __NV_SATFINITE, __NV_E4M3);
+            const float2 x = f[2 * h + i];
+            const float2 q = make_float2(quant_quotient(x.x, scale), quant_quotient(x.y, scale));
+            const __nv_fp8x2_storage_t s = __nv_cvt_float2_to_fp8x2(q, __NV_SATFINITE, __NV_E4M3);
             word |= static_cast<uint32_t>(s) << (16 * i);
         }
         w[h] = word;
@@ -105,105 +136,127 @@ __device__ __forceinline__ float half_warp_max(float v) {
 }
 
 template <int MODE, int PASSES>
-__global__ void __launch_bounds__(kThreads)
-row_norm_quant_kernel(RowArgs a) {
-    const int64_t m = blockIdx.x;
+__global__ void __launch_bounds__(kThreads, min_blocks_per_sm(PASSES))
+row_norm_quant_kernel(const RowArgs a) {
     const int t = threadIdx.x;
     const int lane = t & 31, warp = t >> 5;
 
-    float x[PASSES][8];
+    // Fixed role of each of this thread's chunks (same for every row).
     bool is_q[PASSES], live[PASSES];
-    int col[PASSES];  // first column (within q or within kv) of the chunk
-
-    // Issue every load of the row before touching any value.
-    uint4 raw[PASSES];
+    int col[PASSES];
 #pragma unroll
     for (int p = 0; p < PASSES; ++p) {
         const int c = p * kThreads + t;
         is_q[p] = c < a.cq;
         live[p] = c < a.cq + a.ckv;
         col[p] = (is_q[p] ? c : c - a.cq) * kChunk;
-        raw[p] = make_uint4(0, 0, 0, 0);
-        if (live[p]) {
-            const __nv_bfloat16* src = is_q[p] ? a.q + m * a.ldq + col[p]
-                                               : a.kv + m * a.ldkv + col[p];
-            raw[p] = __ldg(reinterpret_cast<const uint4*>(src));
-        }
     }
 
-    if (MODE != kQuantOnly) {
-        float ssq_q = 0.f, ssq_kv = 0.f;
-#pragma unroll
-        for (int p = 0; p < PASSES; ++p) {
-            unpack8(raw[p], x[p]);
-            float s = 0.f;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) s = fmaf(x[p][i], x[p][i], s);
-            if (is_q[p]) ssq_q += s; else ssq_kv += s;   // dead chunks hold zeros
-        }
-        ssq_q = warp_sum(ssq_q);
-        ssq_kv = warp_sum(ssq_kv);
-        __shared__ float red[2][kThreads / 32];
-        if (lane == 0) { red[0][warp] = ssq_q; red[1][warp] = ssq_kv; }
-        __syncthreads();
-        ssq_q = (red[0][0] + red[0][1]) + (red[0][2] + red[0][3]);
-        ssq_kv = (red[1][0] + red[1][1]) + (red[1][2] + red[1][3]);
-        // Correctly rounded sqrt and divide (not the approximate rsqrt).
-        const float r_q = 1.0f / sqrtf(ssq_q / a.kq_f + a.eps);
-        const float r_kv = 1.0f / sqrtf(ssq_kv / a.kkv_f + a.eps);
-
-        // Gamma chunks follow the same chunk index as the row data.
-#pragma unroll
-        for (int p = 0; p < PASSES; ++p) {
-            if (!live[p]) continue;
-            const __nv_bfloat16* gsrc = is_q[p] ? a.gamma_q + col[p] : a.gamma_kv + col[p];
-            float g[8];
-            unpack8(__ldg(reinterpret_cast<const uint4*>(gsrc)), g);
-            const float r = is_q[p] ? r_q : r_kv;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) x[p][i] = (x[p][i] * r) * g[i];
-        }
-    } else {
-#pragma unroll
-        for (int p = 0; p < PASSES; ++p) unpack8(raw[p], x[p]);
-    }
-
+    // Gamma, once per CTA, as fp32 pairs.
+    float2 gm[PASSES][4];
 #pragma unroll
     for (int p = 0; p < PASSES; ++p) {
-        if (MODE == kNormOnly) {
+        uint4 gr = make_uint4(0, 0, 0, 0);
+        if (MODE != kQuantOnly && live[p])
+            gr = __ldg(reinterpret_cast<const uint4*>((is_q[p] ? a.gamma_q : a.gamma_kv) + col[p]));
+        unpack8(gr, gm[p]);
+    }
+
+    auto load_row = [&](int64_t m, uint4 (&raw)[PASSES]) {
+#pragma unroll
+        for (int p = 0; p < PASSES; ++p) {
+            raw[p] = make_uint4(0, 0, 0, 0);
+            if (live[p]) {
+                const __nv_bfloat16* src = is_q[p] ? a.q + m * a.ldq + col[p] : a.kv + m * a.ldkv + col[p];
+                raw[p] = __ldg(reinterpret_cast<const uint4*>(src));
+            }
+        }
+    };
+
+    __shared__ float red[2][2][kThreads / 32];   // [row parity][q, kv][warp]
+    uint4 cur[PASSES];
+    int64_t m = blockIdx.x;
+    if (m < a.M) load_row(m, cur);
+    int par = 0;
+    for (; m < a.M; m += gridDim.x, par ^= 1) {
+        // Prefetch the next row of this CTA while this one is processed.
+        uint4 nxt[PASSES];
+        const int64_t mn = m + gridDim.x;
+        if (mn < a.M) load_row(mn, nxt);
+
+        float2 x[PASSES][4];
+#pragma unroll
+        for (int p = 0; p < PASSES; ++p) unpack8(cur[p], x[p]);
+
+        if (MODE != kQuantOnly) {
+            float2 sq = make_float2(0.f, 0.f), skv = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int p = 0; p < PASSES; ++p) {
+                float2 s2 = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) s2 = fma2(x[p][i], x[p][i], s2);
+                if (is_q[p]) { sq.x += s2.x; sq.y += s2.y; }    // dead chunks hold zeros
+                else { skv.x += s2.x; skv.y += s2.y; }
+            }
+            float ssq_q = warp_sum(sq.x + sq.y);
+            float ssq_kv = warp_sum(skv.x + skv.y);
+            if (lane == 0) { red[par][0][warp] = ssq_q; red[par][1][warp] = ssq_kv; }
+            __syncthreads();
+            ssq_q = (red[par][0][0] + red[par][0][1]) + (red[par][0][2] + red[par][0][3]);
+            ssq_kv = (red[par][1][0] + red[par][1][1]) + (red[par][1][2] + red[par][1][3]);
+            // Correctly rounded sqrt and divide (not the approximate rsqrt).
+            const float r_q = 1.0f / sqrtf(ssq_q / a.kq_f + a.eps);
+            const float r_kv = 1.0f / sqrtf(ssq_kv / a.kkv_f + a.eps);
+#pragma unroll
+            for (int p = 0; p < PASSES; ++p) {
+                const float r = is_q[p] ? r_q : r_kv;
+                const float2 r2 = make_float2(r, r);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) x[p][i] = mul2(mul2(x[p][i], r2), gm[p][i]);
+            }
+        }
+
+#pragma unroll
+        for (int p = 0; p < PASSES; ++p) {
+            if (MODE == kNormOnly) {
+                if (!live[p]) continue;
+                if (is_q[p])
+                    *reinterpret_cast<uint4*>(a.q_bf16 + m * a.ldq_out + col[p]) = pack8_bf16(x[p]);
+                else
+                    *reinterpret_cast<uint4*>(a.kv_out + m * a.ldkv_out + col[p]) = pack8_bf16(x[p]);
+                continue;
+            }
+            // Group amax: every aligned half-warp of this pass holds one q group,
+            // or kv / dead chunks whose result is discarded.  All lanes shuffle.
+            float amax = 0.f;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) amax = fmaxf(amax, fmaxf(fabsf(x[p][i].x), fabsf(x[p][i].y)));
+            amax = half_warp_max(amax);
             if (!live[p]) continue;
             if (is_q[p]) {
-                *reinterpret_cast<uint4*>(a.q_bf16 + m * a.ldq_out + col[p]) = pack8_bf16(x[p]);
-            } else {
+                const float scale = amax / kE4M3Max;      // IEEE fp32 divide
+                *reinterpret_cast<uint2*>(a.q_fp8 + m * a.ldq_out + col[p]) = pack8_e4m3(x[p], scale);
+                if ((lane & 15) == 0)
+                    a.scale[m * a.scale_row_stride + (col[p] / 128) * a.scale_group_stride] = scale;
+            } else if (MODE == kFused) {
                 *reinterpret_cast<uint4*>(a.kv_out + m * a.ldkv_out + col[p]) = pack8_bf16(x[p]);
             }
-            continue;
         }
-        // Group amax: every aligned half-warp of this pass holds one q group,
-        // or kv / dead chunks whose result is discarded.  All lanes shuffle.
-        float amax = 0.f;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(x[p][i]));
-        amax = half_warp_max(amax);
-        if (!live[p]) continue;
-        if (is_q[p]) {
-            const float inv = amax > 0.f ? kE4M3Max / amax : 0.f;
-            *reinterpret_cast<uint2*>(a.q_fp8 + m * a.ldq_out + col[p]) = pack8_e4m3(x[p], inv);
-            if ((lane & 15) == 0) {
-                const int g = col[p] / 128;
-                a.scale[m * a.scale_row_stride + g * a.scale_group_stride] = amax / kE4M3Max;
-            }
-        } else if (MODE == kFused) {
-            *reinterpret_cast<uint4*>(a.kv_out + m * a.ldkv_out + col[p]) = pack8_bf16(x[p]);
-        }
+        for (int p = 0; p < PASSES; ++p) cur[p] = nxt[p];
     }
 }
 
 template <int MODE>
-static dsnq_status launch_rows(const RowArgs& a, int64_t M, cudaStream_t s) {
+static dsnq_status launch_rows(RowArgs a, int64_t M, cudaStream_t s) {
     const int chunks = a.cq + a.ckv;
     const int passes = (chunks + kThreads - 1) / kThreads;
-    dim3 grid(static_cast<unsigned>(M)), block(kThreads);
+    a.M = M;
+    // Enough CTAs to fill every SM at the register-limited occupancy; each
+    // walks its rows with a grid stride.
+    const int sms = device_sm_count();
+    const int64_t cap = sms > 0 ? static_cast<int64_t>(sms) * min_blocks_per_sm(passes) : M;
+    dim3 grid(static_cast<unsigned>(M < cap ? M : cap)), block(kThreads);
     switch (passes) {
         case 1: row_norm_quant_kernel<MODE, 1><<<grid, block, 0, s>>>(a); break;
         case 2: row_norm_quant_kernel<MODE, 2><<<grid, block, 0, s>>>(a); break;
@@ -244,15 +297,18 @@ weight_block_quant_kernel(int64_t N, int64_t K, const float* __restrict__ w, int
     amax = red[0];
 #pragma unroll
     for (int i = 1; i < 8; ++i) amax = fmaxf(amax, red[i]);
-    const float inv = amax > 0.f ? kE4M3Max / amax : 0.f;
-    if (t == 0) sw[nb * ldsw + kb] = amax / kE4M3Max;
+    const float scale = amax / kE4M3Max;
+    if (t == 0) sw[nb * ldsw + kb] = scale;
     if (!live) return;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {  // 16 codes per 16-byte store
-        float f0[8], f1[8];
+        float2 f0[4], f1[4];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) { f0[i] = v[16 * j + i]; f1[i] = v[16 * j + 8 + i]; }
-        uint2 lo = pack8_e4m3(f0, inv), hi = pack8_e4m3(f1, inv);
+        for (int i = 0; i < 4; ++i) {
+            f0[i] = make_float2(v[16 * j + 2 * i], v[16 * j + 2 * i + 1]);
+            f1[i] = make_float2(v[16 * j + 8 + 2 * i], v[16 * j + 8 + 2 * i + 1]);
+        }
+        uint2 lo = pack8_e4m3(f0, scale), hi = pack8_e4m3(f1, scale);
         *reinterpret_cast<uint4*>(out + row * ldo + c0 + 16 * j) = make_uint4(lo.x, lo.y, hi.x, hi.y);
     }
 }
@@ -261,16 +317,21 @@ weight_block_quant_kernel(int64_t N, int64_t K, const float* __restrict__ w, int
 
 using namespace dsnq;
 
-static dsnq_status check_norm_inputs(int64_t M, int64_t Kq, int64_t Kkv, const void* q, int64_t ldq,
-                                     const void* kv, int64_t ldkv, const void* gq, const void* gkv,
-                                     float eps) {
+// Shape checks come first and M == 0 is accepted before any pointer check, so
+// empty tensors (whose data pointer may be NULL) are a valid no-op.
+static dsnq_status check_norm_shape(int64_t M, int64_t Kq, int64_t Kkv, float eps) {
     if (M < 0 || Kq <= 0 || Kkv <= 0) return DSNQ_ERR_INVALID_ARG;
-    if (!q || !kv || !gq || !gkv) return DSNQ_ERR_INVALID_ARG;
-    if (ldq < Kq || ldkv < Kkv) return DSNQ_ERR_INVALID_ARG;
-    if (!(eps >= 0.f) || eps != eps || eps > 3.0e38f) return DSNQ_ERR_INVALID_ARG;
+    if (!(eps >= 0.f) || eps > 3.0e38f) return DSNQ_ERR_INVALID_ARG;   // also rejects NaN
     if (Kq % 128 != 0 || Kkv % 8 != 0) return DSNQ_ERR_UNSUPPORTED;
     if ((Kq / 8 + Kkv / 8) > 4 * kThreads) return DSNQ_ERR_UNSUPPORTED;
     if (M > 0x7fffffffLL) return DSNQ_ERR_UNSUPPORTED;
+    return DSNQ_OK;
+}
+
+static dsnq_status check_norm_inputs(int64_t Kq, int64_t Kkv, const void* q, int64_t ldq,
+                                     const void* kv, int64_t ldkv, const void* gq, const void* gkv) {
+    if (!q || !kv || !gq || !gkv) return DSNQ_ERR_INVALID_ARG;
+    if (ldq < Kq || ldkv < Kkv) return DSNQ_ERR_INVALID_ARG;
     if (!aligned(q, 16) || !aligned(kv, 16) || !aligned(gq, 16) || !aligned(gkv, 16))
         return DSNQ_ERR_MISALIGNED;
     if (ldq % 8 || ldkv % 8) return DSNQ_ERR_MISALIGNED;
@@ -288,17 +349,19 @@ extern "C" dsnq_status dsnq_fused_dual_rmsnorm_group_quant(
     const void* gamma_q, const void* gamma_kv, float eps, int32_t group,
     void* q_fp8, int64_t ldq_out, float* q_scale, dsnq_scale_layout layout, int64_t ld_scale,
     void* kv_out, int64_t ldkv_out, void* stream) {
-    dsnq_status st = check_norm_inputs(M, Kq, Kkv, q, ldq, kv, ldkv, gamma_q, gamma_kv, eps);
+    dsnq_status st = check_norm_shape(M, Kq, Kkv, eps);
     if (st != DSNQ_OK) return st;
     if (layout != DSNQ_SCALE_ROW_MAJOR && layout != DSNQ_SCALE_COL_MAJOR) return DSNQ_ERR_INVALID_ARG;
     if (group != 128) return DSNQ_ERR_UNSUPPORTED;
+    if (M == 0) return DSNQ_OK;
+    st = check_norm_inputs(Kq, Kkv, q, ldq, kv, ldkv, gamma_q, gamma_kv);
+    if (st != DSNQ_OK) return st;
     if (!q_fp8 || !q_scale || !kv_out) return DSNQ_ERR_INVALID_ARG;
     if (ldq_out < Kq || ldkv_out < Kkv) return DSNQ_ERR_INVALID_ARG;
     const int64_t ld = scale_ld(layout, M, Kq / 128, ld_scale);
     if (ld < 0) return DSNQ_ERR_INVALID_ARG;
     if (!aligned(q_fp8, 8) || ldq_out % 8 || !aligned(kv_out, 16) || ldkv_out % 8 || !aligned(q_scale, 4))
         return DSNQ_ERR_MISALIGNED;
-    if (M == 0) return DSNQ_OK;
     RowArgs a{};
     a.q = static_cast<const __nv_bfloat16*>(q);
     a.kv = static_cast<const __nv_bfloat16*>(kv);
@@ -322,13 +385,15 @@ extern "C" dsnq_status dsnq_dual_rmsnorm_bf16(
     const void* q, int64_t ldq, const void* kv, int64_t ldkv,
     const void* gamma_q, const void* gamma_kv, float eps,
     void* q_out, int64_t ldq_out, void* kv_out, int64_t ldkv_out, void* stream) {
-    dsnq_status st = check_norm_inputs(M, Kq, Kkv, q, ldq, kv, ldkv, gamma_q, gamma_kv, eps);
+    dsnq_status st = check_norm_shape(M, Kq, Kkv, eps);
+    if (st != DSNQ_OK) return st;
+    if (M == 0) return DSNQ_OK;
+    st = check_norm_inputs(Kq, Kkv, q, ldq, kv, ldkv, gamma_q, gamma_kv);
     if (st != DSNQ_OK) return st;
     if (!q_out || !kv_out) return DSNQ_ERR_INVALID_ARG;
     if (ldq_out < Kq || ldkv_out < Kkv) return DSNQ_ERR_INVALID_ARG;
     if (!aligned(q_out, 16) || ldq_out % 8 || !aligned(kv_out, 16) || ldkv_out % 8)
         return DSNQ_ERR_MISALIGNED;
-    if (M == 0) return DSNQ_OK;
     RowArgs a{};
     a.q = static_cast<const __nv_bfloat16*>(q);
     a.kv = static_cast<const __nv_bfloat16*>(kv);
@@ -349,16 +414,17 @@ extern "C" dsnq_status dsnq_group_quant_bf16(
     int64_t M, int64_t K, const void* x, int64_t ldx, int32_t group,
     void* x_fp8, int64_t ldx_out, float* x_scale, dsnq_scale_layout layout, int64_t ld_scale,
     void* stream) {
-    if (M < 0 || K <= 0 || !x || !x_fp8 || !x_scale) return DSNQ_ERR_INVALID_ARG;
-    if (ldx < K || ldx_out < K) return DSNQ_ERR_INVALID_ARG;
+    if (M < 0 || K <= 0) return DSNQ_ERR_INVALID_ARG;
     if (layout != DSNQ_SCALE_ROW_MAJOR && layout != DSNQ_SCALE_COL_MAJOR) return DSNQ_ERR_INVALID_ARG;
     if (group != 128 || K % 128 != 0 || K / 8 > 4 * kThreads) return DSNQ_ERR_UNSUPPORTED;
     if (M > 0x7fffffffLL) return DSNQ_ERR_UNSUPPORTED;
+    if (M == 0) return DSNQ_OK;
+    if (!x || !x_fp8 || !x_scale) return DSNQ_ERR_INVALID_ARG;
+    if (ldx < K || ldx_out < K) return DSNQ_ERR_INVALID_ARG;
     const int64_t ld = scale_ld(layout, M, K / 128, ld_scale);
     if (ld < 0) return DSNQ_ERR_INVALID_ARG;
     if (!aligned(x, 16) || ldx % 8 || !aligned(x_fp8, 8) || ldx_out % 8 || !aligned(x_scale, 4))
         return DSNQ_ERR_MISALIGNED;
-    if (M == 0) return DSNQ_OK;
     RowArgs a{};
     a.q = static_cast<const __nv_bfloat16*>(x);
     a.ldq = ldx;
@@ -373,12 +439,13 @@ extern "C" dsnq_status dsnq_group_quant_bf16(
 extern "C" dsnq_status dsnq_quantize_weight_block128(
     int64_t N, int64_t K, const float* w, int64_t ldw, void* w_fp8, int64_t ldw_out,
     float* w_scale, int64_t ld_wscale, void* stream) {
-    if (N < 0 || K <= 0 || !w || !w_fp8 || !w_scale) return DSNQ_ERR_INVALID_ARG;
-    if (ldw < K || ldw_out < K || ld_wscale < K / 128) return DSNQ_ERR_INVALID_ARG;
+    if (N < 0 || K <= 0) return DSNQ_ERR_INVALID_ARG;
     if (K % 128 != 0) return DSNQ_ERR_UNSUPPORTED;
+    if (N == 0) return DSNQ_OK;
+    if (!w || !w_fp8 || !w_scale) return DSNQ_ERR_INVALID_ARG;
+    if (ldw < K || ldw_out < K || ld_wscale < K / 128) return DSNQ_ERR_INVALID_ARG;
     if (!aligned(w, 16) || ldw % 4 || !aligned(w_fp8, 16) || ldw_out % 16 || !aligned(w_scale, 4))
         return DSNQ_ERR_MISALIGNED;
-    if (N == 0) return DSNQ_OK;
     const int64_t nb = (N + 127) / 128;
     if (nb > 65535) return DSNQ_ERR_UNSUPPORTED;
     dim3 grid(static_cast<unsigned>(K / 128), static_cast<unsigned>(nb));

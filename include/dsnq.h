@@ -29,7 +29,8 @@
  *     call enqueues nothing and returns the status; DSNQ_ERR_CUDA means a
  *     launch was attempted and the CUDA runtime reported an error (the
  *     runtime's last-error state is cleared).
- *   - M == 0 is valid and enqueues nothing.
+ *   - M == 0 (N == 0 for the weight quantizer) is valid and enqueues
+ *     nothing; the data pointers of such empty calls may be NULL.
  */
 #ifndef DSNQ_H_
 #define DSNQ_H_

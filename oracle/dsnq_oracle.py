@@ -14,9 +14,9 @@ RMSNorm + q FP8 per-1x128 group quant", and of sglang PR #27289,
      (PR #53540 body, "Purpose": both latents are RMSNormed with fp32
      accumulation).  Here everything is fp64.
   2. Per-1x128 dynamic group quantization of the normalized q latent to FP8
-     E4M3FN with fp32 scales, taken from the unrounded normalized values
-     (PR #53540 body, "Purpose": quantization reads the fp32 accumulator,
-     single rounding).
+     E4M3FN with fp32 scales, taken from the fp32 normalized values, not from
+     a bf16 copy (PR #53540 body, "Purpose": quantization reads the fp32
+     accumulator, single rounding).
   3. The normalized kv latent rounded to bf16 (PR #53540 prhub summary,
      custom-op snippet: kv_normed has kv's dtype).
   4. The scales written row-major [M, Kq/128] or column-major, element
@@ -32,8 +32,11 @@ RMSNorm + q FP8 per-1x128 group quant", and of sglang PR #27289,
 Readings where the pages are silent (each is also listed in the design notes):
   * RMSNorm is x / sqrt(mean(x^2) + eps) * gamma, eps inside the root, one
     eps for both latents (the shared-path snippet passes self.eps to both).
-  * The scale is amax / 448 (448 = largest finite E4M3FN value), rounded to
-    fp32; an all-zero group gets scale 0 and zero codes (sign kept).
+  * The scale is amax / 448 (448 = largest finite E4M3FN value) in fp32; an
+    all-zero group gets scale 0 and zero codes (sign kept).
+  * The quantize step works on fp32 operands, as the pages place it ("reads
+    the fp32 accumulator"): the normalized value is rounded to fp32 and the
+    quotient x / scale is one IEEE fp32 division before the E4M3 rounding.
   * E4M3FN encoding rounds to nearest, ties to even, and saturates to +-448.
   * The weight-scale tensor (weight_scale or weight_scale_inv) multiplies.
 
@@ -133,23 +136,28 @@ def rmsnorm_f64(x: np.ndarray, gamma: np.ndarray, eps: float) -> np.ndarray:
 
 
 def group_quant_f64(xhat: np.ndarray, group: int = GROUP):
-    """Per-1x`group` quantization of fp64 values to E4M3FN.
+    """Per-1x`group` quantization to E4M3FN of values that the method holds
+    in fp32 (the normalized latent "read from the fp32 accumulator", PR #53540
+    "Purpose"; a bf16 tensor; an fp32 weight).
 
     Returns (codes uint8 [M, K], scales float32 [M, K/group] logical).
-    scale = fp32(amax / 448); code = e4m3(x / scale); amax == 0 gives scale 0
-    and the quotient is taken as x * 0 (signed zero)."""
-    xhat = np.asarray(xhat, dtype=np.float64)
-    M, K = xhat.shape
+    The quantize step is taken in fp32, the precision the pages give it:
+      x32   = fp32(x)                      (exact for bf16 and fp32 inputs)
+      scale = fp32(max|x32| / 448)
+      code  = e4m3(fp32(x32 / scale))      (IEEE fp32 divide, then RNE to E4M3)
+    A group whose scale is 0 gets the quotient x * 0 (signed zero)."""
+    x32 = np.asarray(xhat, dtype=np.float64).astype(np.float32)
+    M, K = x32.shape
     if K % group:
         raise ValueError("K must be a multiple of the group size")
-    g = xhat.reshape(M, K // group, group)
+    g = x32.reshape(M, K // group, group)
     amax = np.max(np.abs(g), axis=-1)
-    scale = (amax / E4M3_MAX).astype(np.float32)
-    s64 = scale.astype(np.float64)[..., None]
-    safe = np.where(s64 > 0, s64, 1.0)
-    quot = np.where(s64 > 0, g / safe, g * 0.0)
-    codes = e4m3_encode(quot).reshape(M, K)
-    return codes, scale
+    scale = amax / np.float32(E4M3_MAX)              # fp32 / fp32: one IEEE rounding
+    s = scale[..., None]
+    safe = np.where(s > 0, s, np.float32(1.0))
+    quot = np.where(s > 0, g / safe, g * np.float32(0.0))   # fp32 quotient
+    codes = e4m3_encode(quot.astype(np.float64)).reshape(M, K)
+    return codes, scale.astype(np.float32)
 
 
 def store_scales(scale: np.ndarray, layout: int, ld: int | None = None) -> np.ndarray:
@@ -235,8 +243,9 @@ def group_quant_bf16(x_bits, group: int = GROUP):
 def quantize_weight_block128(w: np.ndarray):
     """Per-128x128-block quantization of a weight [N, K] (fp32 values) to
     E4M3FN codes with fp32 block scales [ceil(N/128), K/128].  Same rule as the
-    activation groups: scale = fp32(amax/448), code = e4m3(w / scale)."""
-    w = np.asarray(w, dtype=np.float64)
+    activation groups, in fp32: scale = fp32(amax/448),
+    code = e4m3(fp32(w / scale))."""
+    w = np.asarray(w, dtype=np.float32)
     N, K = w.shape
     if K % GROUP:
         raise ValueError("K must be a multiple of 128")
@@ -248,10 +257,10 @@ def quantize_weight_block128(w: np.ndarray):
         for j in range(kb):
             cols = slice(j * GROUP, (j + 1) * GROUP)
             blk = w[rows, cols]
-            s = np.float32(np.max(np.abs(blk)) / E4M3_MAX)
+            s = np.max(np.abs(blk)) / np.float32(E4M3_MAX)
             scale[i, j] = s
-            quot = blk / np.float64(s) if s > 0 else blk * 0.0
-            codes[rows, cols] = e4m3_encode(quot)
+            quot = blk / s if s > 0 else blk * np.float32(0.0)
+            codes[rows, cols] = e4m3_encode(quot.astype(np.float64))
     return codes, scale
 
 

@@ -68,6 +68,7 @@ def fused(lib, **kw):
 
 def test_fused_argument_checks(lib):
     assert fused(lib, M=0) == OK                     # no rows: nothing enqueued
+    assert fused(lib, M=0, q=None, kv=None, qo=None, qs=None, kvo=None) == OK
     assert fused(lib, M=-1) == INVALID
     assert fused(lib, q=None) == INVALID
     assert fused(lib, qs=None) == INVALID
@@ -99,15 +100,16 @@ def gemm(lib, **kw):
 def test_gemm_argument_checks(lib):
     assert gemm(lib) == OK                            # M == 0
     assert gemm(lib, M=4, N=0) == OK
+    assert gemm(lib, a=None, sa=None) == OK          # empty activations may be NULL
     assert gemm(lib, M=-1) == INVALID
-    assert gemm(lib, a=None) == INVALID
+    assert gemm(lib, M=4, a=None) == INVALID
     assert gemm(lib, K=1000, lda=1000, ldw=1000) == UNSUPPORTED
-    assert gemm(lib, N=520, ldo=520) == UNSUPPORTED   # N % 16
-    assert gemm(lib, lda=1000) == INVALID
-    assert gemm(lib, ldsw=11) == INVALID
-    assert gemm(lib, a=A + 8) == MISALIGNED
-    assert gemm(lib, lda=1544) == MISALIGNED
-    assert gemm(lib, o=A + 2) == MISALIGNED
+    assert gemm(lib, M=4, N=520, ldo=520) == UNSUPPORTED   # N % 16
+    assert gemm(lib, M=4, lda=1000) == INVALID
+    assert gemm(lib, M=4, ldsw=11) == INVALID
+    assert gemm(lib, M=4, a=A + 8) == MISALIGNED
+    assert gemm(lib, M=4, lda=1544) == MISALIGNED
+    assert gemm(lib, M=4, o=A + 2) == MISALIGNED
     assert gemm(lib, lay=3) == INVALID
 
 

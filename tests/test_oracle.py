@@ -110,7 +110,7 @@ def test_constant_row_closed_form(c):
     xhat = cb / np.sqrt(cb * cb + e)
     codes, scale, kv_out = oracle.fused_dual_rmsnorm_group_quant(q, kv, bf16(np.ones(Kq)), bf16(np.ones(Kkv)), eps)
     assert np.all(codes == (0xFE if c < 0 else 0x7E))
-    assert np.all(scale == np.float32(abs(xhat) / 448.0))
+    assert np.all(scale == np.float32(abs(xhat)) / np.float32(448.0))
     assert np.all(oracle.bf16_bits_to_f64(kv_out) == float(torch.tensor(xhat, dtype=torch.float64).to(torch.bfloat16)))
 
 
@@ -160,15 +160,32 @@ def test_quant_invariants_half_ulp_and_amax():
     s = np.repeat(scale.astype(np.float64), 128, axis=1)
     q = xq / s
     deq = oracle.e4m3_decode(codes)
-    # half an E4M3 ULP of the quotient: spacing 2^(e-3) in binade e, 2^-9 below 2^-6
+    # half an E4M3 ULP of the quotient: spacing 2^(e-3) in binade e, 2^-9 below
+    # 2^-6; the quotient itself is an fp32 value, hence the 2^-23 relative slack
     e = np.floor(np.log2(np.maximum(np.abs(q), 2.0 ** -6)))
     half_ulp = 0.5 * 2.0 ** (e - 3)
-    assert np.all(np.abs(deq - q) <= half_ulp * (1 + 1e-12))
+    assert np.all(np.abs(deq - q) <= half_ulp + np.abs(q) * 2.0 ** -23)
     # amax element of every group maps to +-448
     g = np.abs(xq).reshape(M, K // 128, 128)
     arg = g.argmax(axis=-1)
     top = np.take_along_axis(codes.reshape(M, K // 128, 128), arg[..., None], -1)[..., 0]
     assert np.all((top == 0x7E) | (top == 0xFE))
+
+
+def test_quant_decision_is_taken_on_the_fp32_quotient():
+    # Documents the reading (not a pin): with amax = 3 the scale fp32(3/448)
+    # is inexact, so a quotient that is an exact E4M3 midpoint in real
+    # arithmetic may fall on either side of it in fp64; the code is the E4M3
+    # rounding of the fp32 quotient fp32(x / scale).
+    x = np.zeros((1, 128), np.float64)
+    x[0, 0] = 3.0
+    x[0, 1:] = np.linspace(-3, 3, 127).astype(np.float32).astype(np.float64)
+    codes, scale = oracle.group_quant_f64(x)
+    s = np.float32(3.0) / np.float32(448.0)
+    q32 = x.astype(np.float32) / s
+    assert scale[0, 0] == s
+    assert np.array_equal(codes, oracle.e4m3_encode(q32.astype(np.float64)))
+    assert codes[0, 0] == 0x7E
 
 
 def test_row_and_column_major_scales_are_transposes():
@@ -209,7 +226,7 @@ def test_weight_block_quant_properties():
     for i in range(3):
         for j in range(2):
             blk = w[i * 128:(i + 1) * 128, j * 128:(j + 1) * 128]
-            assert sw[i, j] == np.float32(np.abs(blk).max() / 448.0)
+            assert sw[i, j] == np.abs(blk).max() / np.float32(448.0)
             r, c = np.unravel_index(np.abs(blk).argmax(), blk.shape)
             assert codes[i * 128 + r, j * 128 + c] in (0x7E, 0xFE)
     deq = oracle.dequantize_weight(codes, sw)
