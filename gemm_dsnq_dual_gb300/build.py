@@ -8,6 +8,7 @@ runs on hosts without a GPU.  Run as `python -m gemm_dsnq_dual_gb300.build`.
 from __future__ import annotations
 
 import os
+import platform
 import shutil
 import subprocess
 import sys
@@ -17,7 +18,9 @@ PKG_DIR = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG_DIR)
 CSRC = os.path.join(PKG_DIR, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
-BUILD_DIR = os.path.join(ROOT, "_build")
+# Objects are kept per host architecture, so a tree copied between an x86
+# build host and an Arm GPU host never links foreign objects.
+BUILD_DIR = os.path.join(ROOT, "_build", platform.machine() or "unknown")
 LIB_NAME = "libdsnq.so"
 LIB_PATH = os.path.join(PKG_DIR, LIB_NAME)
 
@@ -74,12 +77,16 @@ def build(verbose: bool = False, force: bool = False, extra_flags=None) -> str:
 
     with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    if force or not _newer(LIB_PATH, objs):
+    stamp = os.path.join(BUILD_DIR, "libdsnq.stamp")   # which objects the library was linked from
+    if force or not _newer(LIB_PATH, objs) or not os.path.exists(stamp) or \
+            open(stamp).read() != LIB_PATH + "\n" + platform.machine():
         cmd = [cc, *ARCH, "-shared", "-o", LIB_PATH + ".tmp", *objs, "-lcudart"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
         os.replace(LIB_PATH + ".tmp", LIB_PATH)
+        with open(stamp, "w") as f:
+            f.write(LIB_PATH + "\n" + platform.machine())
     return LIB_PATH
 
 

@@ -21,9 +21,15 @@
 //     (tcgen05.ld), multiply by sa * sw and add it into fp32 registers while the
 //     MMA of the next K block fills the other buffer.
 //   * Warp roles: warp 0 issues TMA, warp 1 allocates TMEM and issues MMA
-//     (one elected lane), warps 2..9 promote and store.  Warp w may only read
-//     TMEM lanes 32*(w%4)..+31, so warps 2..5 and 6..9 each cover all 128 lanes
-//     and split the tile's columns in two halves.
+//     (one lane), warp 2 is the gate, warps 4.. promote and store.  Any wait
+//     or shared-memory load in the thread that issues tcgen05.mma stalls it
+//     behind the MMAs already in flight (about one K block per wait, measured
+//     on GB300), so the MMA thread performs none in steady state: the gate
+//     thread waits for "stage loaded" and "TMEM buffer free" and publishes a
+//     running count of K blocks ready, which the MMA thread re-reads only when
+//     it has caught up with its last reading.  Warp w may only read TMEM lanes
+//     32*(w%4)..+31, so each group of four promotion warps covers all 128 lanes
+//     and the groups split the tile's columns.
 //   * Orientation.  The MMA's M side ("P", 128 rows) and N side ("Q", BN rows)
 //     are either (activations, weights) for large M, or (weights, activations)
 //     for decode batches (swap-AB): 128 weight rows then fill the MMA rows and
@@ -70,6 +76,7 @@ struct Params {
     int tiles_m;                   // tiles along the activation rows
     int tiles0;                    // tiles of problem 0
     int total_tiles;               // tiles of both problems
+    int vec_scales;                // column-major scales whose columns are 16-byte aligned
     Problem prob[2];
     uint64_t timeout_ns;
     uint32_t inject;
@@ -112,15 +119,37 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// try_wait that lets the hardware suspend the thread until the phase
+// completes or `hint_ns` passes, so a waiting warp takes no issue slots.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
+constexpr uint32_t kSleepHintNs = 100000;   // re-check abort/timeout at least every 100 us
+
 // Bounded wait for the phase of `parity` to complete.  Gives up when another
 // thread of the CTA has raised *abort, or after timeout_ns, in which case it
-// raises *abort and records the timeout in the device status word.
+// raises *abort and records the timeout in the device status word.  SPIN
+// polls (lowest wake-up latency, for the waits on the MMA <-> promotion
+// ring); otherwise the thread sleeps in hardware between polls.
+template <bool SPIN = false>
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort,
                                              uint64_t timeout_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = now_ns();
+    uint32_t n = 0;
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (SPIN ? mbar_try_wait(bar, parity) : mbar_try_wait_sleep(bar, parity, kSleepHintNs)) return true;
+        if (SPIN && (++n & 63)) continue;       // check abort and the clock every 64 polls
+        
         if (*abort) return false;
         if (now_ns() - t0 > timeout_ns) {
             *abort = 1;
@@ -134,8 +163,39 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, vola
 // copies and MMAs land before its shared and tensor memory are released).
 __device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, uint64_t timeout_ns) {
     const uint64_t t0 = now_ns();
-    while (!mbar_try_wait(bar, parity)) {
+    while (!mbar_try_wait_sleep(bar, parity, kSleepHintNs)) {
         if (now_ns() - t0 > timeout_ns) return;
+    }
+}
+
+__device__ __forceinline__ void st_release_shared(uint32_t addr, uint32_t v) {
+    asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_shared(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+// MMA thread: wait until the gate's count exceeds `need` (bounded like
+// wait_bounded); `ready` receives the count read.
+__device__ __forceinline__ bool wait_gate(uint32_t gate, uint32_t need, uint32_t& ready, volatile int* abort,
+                                          uint64_t timeout_ns) {
+    ready = ld_acquire_shared(gate);
+    if (ready > need) return true;
+    const uint64_t t0 = now_ns();
+    uint32_t n = 0;
+    while (true) {
+        ready = ld_acquire_shared(gate);
+        if (ready > need) return true;
+        if (++n & 63) continue;                  // check abort and the clock every 64 polls
+        if (*abort) return false;
+        if (now_ns() - t0 > timeout_ns) {
+            *abort = 1;
+            atomicOr(&g_status, kStatusTimeout);
+            return false;
+        }
     }
 }
 
@@ -146,6 +206,21 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
         " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
         : "memory");
+}
+
+// Tiled bulk store shared -> global (rows past the tensor's extent are clipped).
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int32_t x, int32_t y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(src), "r"(x), "r"(y)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
@@ -175,41 +250,124 @@ __device__ __forceinline__ void tc_mma_f8(uint32_t d_tmem, uint64_t a_desc, uint
         : "memory");
 }
 
-// 32 lanes x N consecutive 32-bit TMEM columns; thread i gets lane (base+i).
+// 32 lanes x N consecutive 32-bit TMEM columns, returned as N/2 column pairs
+// (64-bit registers, ready for the paired f32x2 instructions); thread i gets
+// lane (base+i).  Includes the wait for the load to complete.
 template <int N>
-__device__ __forceinline__ void tmem_ld(uint32_t taddr, uint32_t (&r)[N]);
+__device__ __forceinline__ void tmem_ld_pairs(uint32_t taddr, uint64_t (&r)[N / 2]);
 
 template <>
-__device__ __forceinline__ void tmem_ld<8>(uint32_t taddr, uint32_t (&r)[8]) {
+__device__ __forceinline__ void tmem_ld_pairs<8>(uint32_t taddr, uint64_t (&r)[4]) {
     asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
-        : "r"(taddr));
+        "{\n\t.reg .b32 t<8>;\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {t0, t1, t2, t3, t4, t5, t6, t7}, [%4];\n\t"
+        "tcgen05.wait::ld.sync.aligned;\n\t"
+        "mov.b64 %0, {t0, t1};\n\t"
+        "mov.b64 %1, {t2, t3};\n\t"
+        "mov.b64 %2, {t4, t5};\n\t"
+        "mov.b64 %3, {t6, t7};\n\t"
+        "}"
+        : "=l"(r[0]), "=l"(r[1]), "=l"(r[2]), "=l"(r[3])
+        : "r"(taddr)
+        : "memory");
 }
 
 template <>
-__device__ __forceinline__ void tmem_ld<16>(uint32_t taddr, uint32_t (&r)[16]) {
+__device__ __forceinline__ void tmem_ld_pairs<16>(uint32_t taddr, uint64_t (&r)[8]) {
     asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr));
+        "{\n\t.reg .b32 t<16>;\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {t0, t1, t2, t3, t4, t5, t6, t7, t8, t9, t10, t11, t12, t13, t14, t15}, [%8];\n\t"
+        "tcgen05.wait::ld.sync.aligned;\n\t"
+        "mov.b64 %0, {t0, t1};\n\t"
+        "mov.b64 %1, {t2, t3};\n\t"
+        "mov.b64 %2, {t4, t5};\n\t"
+        "mov.b64 %3, {t6, t7};\n\t"
+        "mov.b64 %4, {t8, t9};\n\t"
+        "mov.b64 %5, {t10, t11};\n\t"
+        "mov.b64 %6, {t12, t13};\n\t"
+        "mov.b64 %7, {t14, t15};\n\t"
+        "}"
+        : "=l"(r[0]), "=l"(r[1]), "=l"(r[2]), "=l"(r[3]), "=l"(r[4]), "=l"(r[5]), "=l"(r[6]), "=l"(r[7])
+        : "r"(taddr)
+        : "memory");
 }
 
 template <>
-__device__ __forceinline__ void tmem_ld<32>(uint32_t taddr, uint32_t (&r)[32]) {
+__device__ __forceinline__ void tmem_ld_pairs<32>(uint32_t taddr, uint64_t (&r)[16]) {
     asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr));
+        "{\n\t.reg .b32 t<32>;\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {t0, t1, t2, t3, t4, t5, t6, t7, t8, t9, t10, t11, t12, t13, t14, t15, t16, t17, t18, t19, t20, t21, t22, t23, t24, t25, t26, t27, t28, t29, t30, t31}, [%16];\n\t"
+        "tcgen05.wait::ld.sync.aligned;\n\t"
+        "mov.b64 %0, {t0, t1};\n\t"
+        "mov.b64 %1, {t2, t3};\n\t"
+        "mov.b64 %2, {t4, t5};\n\t"
+        "mov.b64 %3, {t6, t7};\n\t"
+        "mov.b64 %4, {t8, t9};\n\t"
+        "mov.b64 %5, {t10, t11};\n\t"
+        "mov.b64 %6, {t12, t13};\n\t"
+        "mov.b64 %7, {t14, t15};\n\t"
+        "mov.b64 %8, {t16, t17};\n\t"
+        "mov.b64 %9, {t18, t19};\n\t"
+        "mov.b64 %10, {t20, t21};\n\t"
+        "mov.b64 %11, {t22, t23};\n\t"
+        "mov.b64 %12, {t24, t25};\n\t"
+        "mov.b64 %13, {t26, t27};\n\t"
+        "mov.b64 %14, {t28, t29};\n\t"
+        "mov.b64 %15, {t30, t31};\n\t"
+        "}"
+        : "=l"(r[0]), "=l"(r[1]), "=l"(r[2]), "=l"(r[3]), "=l"(r[4]), "=l"(r[5]), "=l"(r[6]), "=l"(r[7]), "=l"(r[8]), "=l"(r[9]), "=l"(r[10]), "=l"(r[11]), "=l"(r[12]), "=l"(r[13]), "=l"(r[14]), "=l"(r[15])
+        : "r"(taddr)
+        : "memory");
 }
 
-__device__ __forceinline__ void tmem_ld_wait() {
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+template <>
+__device__ __forceinline__ void tmem_ld_pairs<64>(uint32_t taddr, uint64_t (&r)[32]) {
+    asm volatile(
+        "{\n\t.reg .b32 t<64>;\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x64.b32 {t0, t1, t2, t3, t4, t5, t6, t7, t8, t9, t10, t11, t12, t13, t14, t15, t16, t17, t18, t19, t20, t21, t22, t23, t24, t25, t26, t27, t28, t29, t30, t31, t32, t33, t34, t35, t36, t37, t38, t39, t40, t41, t42, t43, t44, t45, t46, t47, t48, t49, t50, t51, t52, t53, t54, t55, t56, t57, t58, t59, t60, t61, t62, t63}, [%32];\n\t"
+        "tcgen05.wait::ld.sync.aligned;\n\t"
+        "mov.b64 %0, {t0, t1};\n\t"
+        "mov.b64 %1, {t2, t3};\n\t"
+        "mov.b64 %2, {t4, t5};\n\t"
+        "mov.b64 %3, {t6, t7};\n\t"
+        "mov.b64 %4, {t8, t9};\n\t"
+        "mov.b64 %5, {t10, t11};\n\t"
+        "mov.b64 %6, {t12, t13};\n\t"
+        "mov.b64 %7, {t14, t15};\n\t"
+        "mov.b64 %8, {t16, t17};\n\t"
+        "mov.b64 %9, {t18, t19};\n\t"
+        "mov.b64 %10, {t20, t21};\n\t"
+        "mov.b64 %11, {t22, t23};\n\t"
+        "mov.b64 %12, {t24, t25};\n\t"
+        "mov.b64 %13, {t26, t27};\n\t"
+        "mov.b64 %14, {t28, t29};\n\t"
+        "mov.b64 %15, {t30, t31};\n\t"
+        "mov.b64 %16, {t32, t33};\n\t"
+        "mov.b64 %17, {t34, t35};\n\t"
+        "mov.b64 %18, {t36, t37};\n\t"
+        "mov.b64 %19, {t38, t39};\n\t"
+        "mov.b64 %20, {t40, t41};\n\t"
+        "mov.b64 %21, {t42, t43};\n\t"
+        "mov.b64 %22, {t44, t45};\n\t"
+        "mov.b64 %23, {t46, t47};\n\t"
+        "mov.b64 %24, {t48, t49};\n\t"
+        "mov.b64 %25, {t50, t51};\n\t"
+        "mov.b64 %26, {t52, t53};\n\t"
+        "mov.b64 %27, {t54, t55};\n\t"
+        "mov.b64 %28, {t56, t57};\n\t"
+        "mov.b64 %29, {t58, t59};\n\t"
+        "mov.b64 %30, {t60, t61};\n\t"
+        "mov.b64 %31, {t62, t63};\n\t"
+        "}"
+        : "=l"(r[0]), "=l"(r[1]), "=l"(r[2]), "=l"(r[3]), "=l"(r[4]), "=l"(r[5]), "=l"(r[6]), "=l"(r[7]), "=l"(r[8]), "=l"(r[9]), "=l"(r[10]), "=l"(r[11]), "=l"(r[12]), "=l"(r[13]), "=l"(r[14]), "=l"(r[15]), "=l"(r[16]), "=l"(r[17]), "=l"(r[18]), "=l"(r[19]), "=l"(r[20]), "=l"(r[21]), "=l"(r[22]), "=l"(r[23]), "=l"(r[24]), "=l"(r[25]), "=l"(r[26]), "=l"(r[27]), "=l"(r[28]), "=l"(r[29]), "=l"(r[30]), "=l"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+
+__device__ __forceinline__ float2 as_float2(uint64_t v) {
+    float2 f;
+    memcpy(&f, &v, sizeof(f));
+    return f;
 }
 
 // Shared-memory matrix descriptor of a K-major tile written by TMA with the
@@ -235,10 +393,6 @@ __host__ __device__ constexpr uint32_t idesc_e4m3(int bn) {
            | (static_cast<uint32_t>(kPRows >> 4) << 24);  // M >> 4
 }
 
-__device__ __forceinline__ void named_bar_sync(int id, int count) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-
 // ------------------------------------------------------------------- kernel
 
 // Compile-time shape of one kernel variant.
@@ -257,14 +411,20 @@ struct Cfg {
                                      : kTmemNeed <= 256 ? 256 : 512;
     static constexpr int kSlices = EPI_WARPS / 4;       // column slices per lane quarter
     static constexpr int kCols = BN / kSlices;          // tile columns per promotion thread
-    static constexpr int kLd = kCols >= 64 ? 32 : (kCols >= 16 ? 16 : kCols);  // columns per tcgen05.ld
-    static constexpr int kThreads = (2 + EPI_WARPS) * 32;
+    static constexpr int kScaleCols = SWAP ? BN : kPRows;  // activation scales per K block in a slot
+    static constexpr int kScaleRegs = SWAP ? kCols / 4 : 1; // float4 of scales a thread needs per K block
+    static_assert(2 * STAGES <= 32, "one producer lane per operand and stage");
+    // Non-swap epilogue: each promotion warp stages its 32 x kCols bf16 block
+    // (rows of kCols*2 = 64 bytes, 64-byte swizzle) for one TMA store.
+    static constexpr int kStageOutBytes = SWAP ? 0 : 32 * kCols * 2;
+    static_assert(SWAP || kCols == 32, "the store box is 32 rows x 64 bytes");
+    static constexpr int kThreads = (4 + EPI_WARPS) * 32;  // producer, MMA, gate, scale loader, promotion
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M=128 is 16..256 step 16");
     static_assert(kTmemNeed <= 512, "TMEM holds 512 fp32 columns");
     static_assert(EPI_WARPS % 4 == 0 && BN % kSlices == 0, "promotion warps tile the accumulator");
-    static_assert(kCols % 8 == 0 && kCols % kLd == 0, "TMEM is read 8 columns at a time at least");
+    static_assert(kCols == 8 || kCols == 16 || kCols == 32 || kCols == 64, "one TMEM load per K block");
     // Non-swap: a thread's columns must share one 128-feature weight-scale block.
-    static_assert(SWAP || (kPRows % kCols == 0), "non-swap slices stay inside a scale block");
+    static_assert(SWAP || BN == kPRows, "non-swap tiles are 128 features wide");
 };
 
 // Tile t of the concatenated tile space -> (problem, first activation row, first feature).
@@ -283,25 +443,37 @@ __global__ void __launch_bounds__(Cfg<BN, SWAP, STAGES, NBUF, EPI_WARPS>::kThrea
 block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                          const __grid_constant__ CUtensorMap map_w0,
                          const __grid_constant__ CUtensorMap map_w1,
+                         const __grid_constant__ CUtensorMap map_o0,
+                         const __grid_constant__ CUtensorMap map_o1,
                          const Params p) {
     using C = Cfg<BN, SWAP, STAGES, NBUF, EPI_WARPS>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 1024-byte alignment for the 128-byte-swizzled tiles.
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* tiles = smem;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * C::kStageBytes);
+    uint8_t* out_stage = smem + STAGES * C::kStageBytes;      // [EPI_WARPS][kStageOutBytes]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(out_stage + EPI_WARPS * C::kStageOutBytes);
     uint64_t* full = bars;                    // [STAGES] TMA -> MMA
     uint64_t* empty = bars + STAGES;          // [STAGES] MMA -> TMA
     uint64_t* tfull = bars + 2 * STAGES;      // [NBUF]   MMA -> promotion
-    uint64_t* tempty = tfull + NBUF;          // [NBUF]   promotion -> MMA
-    uint64_t* drain = tempty + NBUF;          // [1]      abort drain of MMAs
+    uint64_t* tempty = tfull + NBUF;          // [NBUF]   promotion -> gate
+    uint64_t* sfull = tempty + NBUF;          // [2]      scale loader -> promotion
+    uint64_t* sempty = sfull + 2;             // [2]      promotion -> scale loader
+    uint64_t* drain = sempty + 2;             // [1]      abort drain of MMAs
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
-    float* sq = reinterpret_cast<float*>(tmem_holder + 4);  // swap: [KB][BN] combined scales
+    uint32_t* gate = tmem_holder + 2;         // K blocks ready for the MMA thread
+    // Scale slots (16-byte aligned), K blocks padded to KBP = a multiple of 4:
+    // [2][KBP][kScaleCols] raw activation scales (per P row for non-swap, per
+    // token for swap), then [2][KBP] weight scales.
+    const int KBP = (p.KB + 3) & ~3;
+    float* sa_slots = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(tmem_holder + 4) + 15) & ~uintptr_t(15));
+    float* sw_slots = sa_slots + 2 * KBP * C::kScaleCols;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int total = p.total_tiles;
+    const int KB = p.KB;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -312,12 +484,21 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
             mbar_init(smem_u32(&tfull[b]), 1);
             mbar_init(smem_u32(&tempty[b]), EPI_WARPS);
         }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_u32(&sfull[i]), 32);            // one cp.async arrival per loader lane
+            mbar_init(smem_u32(&sempty[i]), EPI_WARPS);
+        }
         mbar_init(smem_u32(drain), 1);
         *abort_flag = 0;
+        *gate = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         tma_prefetch_desc(&map_a);
         tma_prefetch_desc(&map_w0);
         tma_prefetch_desc(&map_w1);
+        if (!SWAP) {
+            tma_prefetch_desc(&map_o0);
+            tma_prefetch_desc(&map_o1);
+        }
     }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_holder)),
@@ -332,64 +513,70 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
     const uint64_t tmo = p.timeout_ns;
 
     if (warp == 0) {
-        // ------------------------------------------------ TMA producer (one lane)
-        if (lane == 0) {
-            uint32_t g = 0;  // K blocks of this CTA so far, across tiles
+        // ------------------------------------------------ TMA producer (2*STAGES lanes)
+        // A thread's bulk copies complete one after another (about one per L2
+        // round trip, measured on GB300), so every stage has its own pair of
+        // lanes, each running its own loop: lane 2s loads the P tile of the K
+        // blocks that use stage s (and arms the stage's barrier), lane 2s+1
+        // their Q tile.  The lanes never wait for one another.
+        if (lane < 2 * STAGES) {
+            const int ntl = blockIdx.x < total ? (total - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+            const uint32_t ng = static_cast<uint32_t>(ntl) * KB;   // K blocks of this CTA
+            const int s = lane >> 1;
+            const bool loads_q = lane & 1;
+            const uint32_t fb = smem_u32(&full[s]);
+            uint8_t* st = tiles + s * C::kStageBytes;
+            uint32_t last = 0;     // 1 + the last K block this lane issued (0: none)
             bool ok = true;
-            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+            for (uint32_t g = s; g < ng; g += STAGES) {
+                if (!wait_bounded(smem_u32(&empty[s]), ((g / STAGES) & 1) ^ 1, abort_flag, tmo)) {
+                    ok = false;
+                    break;
+                }
+                if ((p.inject & 1u) && g == 0) continue;   // test hook: never arrive on full[0]
+                const int tl = static_cast<int>(g / KB), kb = static_cast<int>(g % KB);
                 int pi, m0, n0;
-                tile_coords<BN, SWAP>(p, t, pi, m0, n0);
+                tile_coords<BN, SWAP>(p, blockIdx.x + tl * gridDim.x, pi, m0, n0);
                 const CUtensorMap* map_w = pi ? &map_w1 : &map_w0;
-                const CUtensorMap* map_p = SWAP ? map_w : &map_a;
-                const CUtensorMap* map_q = SWAP ? &map_a : map_w;
-                const int p_row = SWAP ? n0 : m0;
-                const int q_row = SWAP ? m0 : n0;
-                for (int kb = 0; kb < p.KB; ++kb, ++g) {
-                    const int s = g % STAGES;
-                    if (!wait_bounded(smem_u32(&empty[s]), ((g / STAGES) & 1) ^ 1, abort_flag, tmo)) {
-                        ok = false;
-                        break;
-                    }
-                    if ((p.inject & 1u) && g == 0) continue;   // test hook: never arrive on full[0]
-                    const uint32_t fb = smem_u32(&full[s]);
+                if (!loads_q) {
                     mbar_arrive_expect_tx(fb, C::kStageBytes);
-                    uint8_t* st = tiles + s * C::kStageBytes;
-                    tma_load_2d(smem_u32(st), map_p, fb, kb * kBK, p_row);
-                    tma_load_2d(smem_u32(st + C::kPBytes), map_q, fb, kb * kBK, q_row);
+                    tma_load_2d(smem_u32(st), SWAP ? map_w : &map_a, fb, kb * kBK, SWAP ? n0 : m0);
+                } else {
+                    tma_load_2d(smem_u32(st + C::kPBytes), SWAP ? &map_a : map_w, fb, kb * kBK, SWAP ? m0 : n0);
                 }
+                last = g + 1;
             }
-            if (!ok || *abort_flag) {
-                // Let the copies already issued land before the CTA exits.
-                const uint32_t first = g > STAGES ? g - STAGES : 0;
-                for (uint32_t j = first; j < g; ++j) {
-                    if ((p.inject & 1u) && j == 0) continue;
-                    wait_drain(smem_u32(&full[j % STAGES]), (j / STAGES) & 1, tmo);
-                }
+            if ((!ok || *abort_flag) && last > 0) {
+                // Let this lane's last copy land before the CTA exits.
+                const uint32_t g = last - 1;
+                wait_drain(fb, (g / STAGES) & 1, tmo);
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer (one lane)
         constexpr uint32_t idesc = idesc_e4m3(BN);
         if (lane == 0) {
-            uint32_t g = 0;
+            // Descriptors of stage 0; stage s and K slice k only move the start
+            // address field (16-byte units), which stays below 2^14 for 227 KB.
+            const uint64_t dp0 = smem_desc_k_sw128(smem_u32(tiles));
+            const uint64_t dq0 = smem_desc_k_sw128(smem_u32(tiles + C::kPBytes));
+            uint32_t g = 0, ready = 0;
             bool ok = true, any = false;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-                for (int kb = 0; kb < p.KB; ++kb, ++g) {
+                for (int kb = 0; kb < KB; ++kb, ++g) {
                     const int s = g % STAGES;
                     const int b = g % NBUF;
-                    if (!wait_bounded(smem_u32(&full[s]), (g / STAGES) & 1, abort_flag, tmo) ||
-                        !wait_bounded(smem_u32(&tempty[b]), ((g / NBUF) & 1) ^ 1, abort_flag, tmo)) {
+                    if (g >= ready && !wait_gate(smem_u32(gate), g, ready, abort_flag, tmo)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t pa = smem_u32(tiles + s * C::kStageBytes);
-                    const uint32_t qa = pa + C::kPBytes;
+                    const uint64_t so = static_cast<uint64_t>((s * C::kStageBytes) >> 4);
                     const uint32_t d = tmem_base + static_cast<uint32_t>(b * BN);
 #pragma unroll
                     for (int k = 0; k < kBK / kUmmaK; ++k) {
-                        tc_mma_f8(d, smem_desc_k_sw128(pa + k * kUmmaK), smem_desc_k_sw128(qa + k * kUmmaK),
-                                  idesc, k > 0 ? 1u : 0u);
+                        const uint64_t ko = so + static_cast<uint64_t>((k * kUmmaK) >> 4);
+                        tc_mma_f8(d, dp0 + ko, dq0 + ko, idesc, k > 0 ? 1u : 0u);
                     }
                     tc_commit(smem_u32(&empty[s]));    // stage free once these MMAs have read it
                     tc_commit(smem_u32(&tfull[b]));    // partial sum ready
@@ -402,88 +589,205 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
             }
         }
         __syncwarp();
+    } else if (warp == 2) {
+        // ------------------------------------------------ gate (one lane)
+        if (lane == 0) {
+            uint32_t g = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+                for (int kb = 0; kb < KB; ++kb, ++g) {
+                    if (!wait_bounded<true>(smem_u32(&full[g % STAGES]), (g / STAGES) & 1, abort_flag, tmo) ||
+                        !wait_bounded<true>(smem_u32(&tempty[g % NBUF]), ((g / NBUF) & 1) ^ 1, abort_flag, tmo)) {
+                        ok = false;
+                        break;
+                    }
+                    st_release_shared(smem_u32(gate), g + 1);
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 3) {
+        // ------------------------------------------------ scale loader (whole warp)
+        // Raw activation scales of every K block of the CTA's next tile (per P
+        // row, or per token for swap) and the tile's weight-scale row, copied
+        // with cp.async into one of two shared slots; the slot's barrier
+        // completes when every lane's copies have landed.
+        int i = 0;
+        for (int t = blockIdx.x; t < total; t += gridDim.x, ++i) {
+            const int slot = i & 1;
+            const bool got = wait_bounded(smem_u32(&sempty[slot]), ((i >> 1) & 1) ^ 1, abort_flag, tmo);
+            if (!__all_sync(0xffffffffu, got)) break;
+            int pi, m0, n0;
+            tile_coords<BN, SWAP>(p, t, pi, m0, n0);
+            const Problem pr = pi ? p.prob[1] : p.prob[0];
+            const float* sw = pr.w_scale + static_cast<int64_t>(n0 / kPRows) * pr.ld_ws;
+            float* sa_dst = sa_slots + slot * KBP * C::kScaleCols;   // [kb][kScaleCols]
+            const int rows = p.M - m0 < C::kScaleCols ? p.M - m0 : C::kScaleCols;
+            if (p.vec_scales && rows == C::kScaleCols) {
+                // Column-major scales with 16-byte aligned columns: each K block's
+                // run of kScaleCols scales is contiguous, 16 bytes per lane per copy
+                // (few, large copies: a thread's copies complete one at a time).
+                constexpr int kVec = C::kScaleCols / 4;
+                for (int e = lane; e < KB * kVec; e += 32) {
+                    const int kb = e / kVec, v = e % kVec;
+                    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(sa_dst + kb * C::kScaleCols + 4 * v)),
+                                 "l"(p.a_scale + static_cast<int64_t>(kb) * p.as_gs + m0 + 4 * v)
+                                 : "memory");
+                }
+            } else {
+                for (int e = lane; e < KB * C::kScaleCols; e += 32) {
+                    const int kb = e / C::kScaleCols, j = e % C::kScaleCols;   // lanes walk rows: coalesced reads
+                    const int m = m0 + j;
+                    const bool live = m < p.M;                 // zero fill past the last row
+                    const float* src = live ? p.a_scale + static_cast<int64_t>(m) * p.as_rs + kb * p.as_gs : p.a_scale;
+                    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(sa_dst + e)), "l"(src),
+                                 "r"(live ? 4 : 0)
+                                 : "memory");
+                }
+            }
+            for (int kb = lane; kb < KB; kb += 32)
+                asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(sw_slots + slot * KBP + kb)),
+                             "l"(sw + kb)
+                             : "memory");
+            asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(&sfull[slot]))
+                         : "memory");
+        }
+        asm volatile("cp.async.wait_all;" ::: "memory");   // no copy outlives the CTA
     } else {
         // ------------------------------------------------ promotion + store
-        const int ew = warp - 2;                 // 0 .. EPI_WARPS-1
+        const int ew = warp - 4;                 // 0 .. EPI_WARPS-1
         const int quarter = warp & 3;            // TMEM lanes 32*quarter .. +31
         const int slice = ew >> 2;               // column slice of the tile
         const int row = quarter * 32 + lane;     // P row (TMEM lane)
         const int col0 = slice * C::kCols;
         uint32_t g = 0;
         bool ok = true;
-        for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        int i = 0;
+        for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++i) {
             int pi, m0, n0;
             tile_coords<BN, SWAP>(p, t, pi, m0, n0);
             const Problem pr = pi ? p.prob[1] : p.prob[0];
-            if (SWAP) {
-                // Combined scale sa(m0+j, kb) * sw[n0/128, kb] for every token j of the tile.
-                named_bar_sync(1, EPI_WARPS * 32);     // previous tile's readers are done
-                const int nb = n0 / kPRows;
-                for (int i = threadIdx.x - 64; i < p.KB * BN; i += EPI_WARPS * 32) {
-                    const int kb = i / BN, j = i % BN;
-                    const int m = m0 + j;
-                    float v = 0.f;
-                    if (m < p.M) v = p.a_scale[m * p.as_rs + kb * p.as_gs] * pr.w_scale[nb * pr.ld_ws + kb];
-                    sq[i] = v;
-                }
-                named_bar_sync(1, EPI_WARPS * 32);
+            const int slot = i & 1;
+            {
+                const bool got = wait_bounded(smem_u32(&sfull[slot]), (i >> 1) & 1, abort_flag, tmo);
+                if (!__all_sync(0xffffffffu, got)) break;
             }
+            const float* sa_t = sa_slots + slot * KBP * C::kScaleCols + (SWAP ? col0 : row);
+            const float* sw_t = sw_slots + slot * KBP;
 
-            float acc[C::kCols];
+            float2 acc[C::kCols / 2];
 #pragma unroll
-            for (int j = 0; j < C::kCols; ++j) acc[j] = 0.f;
-            const int m_row = m0 + row;                       // non-swap: token of this thread
-            const int nb_ns = (n0 + col0) / kPRows;           // non-swap: scale block of the slice
+            for (int j = 0; j < C::kCols / 2; ++j) acc[j] = make_float2(0.f, 0.f);
 
-            for (int kb = 0; kb < p.KB; ++kb, ++g) {
+            // One K block: wait for its partial sum, read it out of TMEM, hand
+            // the buffer back, and add it in with the per-column scales sc[j]
+            // (pairs).  No shared-memory access here beyond the barriers: the
+            // scales arrive in registers, fetched ahead of use, because shared
+            // loads are slow while the tensor core streams its operands.
+            auto promote = [&](const float2* sc, bool uniform) -> bool {
                 const int b = g % NBUF;
-                float srow = 0.f;
-                if (!SWAP && m_row < p.M)
-                    srow = p.a_scale[m_row * p.as_rs + kb * p.as_gs] * pr.w_scale[nb_ns * pr.ld_ws + kb];
                 // Every lane polls (each acquires the phase); the outcome is made
-                // warp-uniform before the warp-collective TMEM loads.
-                const bool got = wait_bounded(smem_u32(&tfull[b]), (g / NBUF) & 1, abort_flag, tmo);
-                if (!__all_sync(0xffffffffu, got)) {
-                    ok = false;
-                    break;
-                }
+                // warp-uniform before the warp-collective TMEM load.
+                const bool got = wait_bounded<true>(smem_u32(&tfull[b]), (g / NBUF) & 1, abort_flag, tmo);
+                if (!__all_sync(0xffffffffu, got)) return false;
                 tc_fence_after();
-                const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
-                                       static_cast<uint32_t>(b * BN + col0);
+                uint64_t r[C::kCols / 2];
+                tmem_ld_pairs<C::kCols>(tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                            static_cast<uint32_t>(b * BN + col0),
+                                        r);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&tempty[b]));
 #pragma unroll
-                for (int c = 0; c < C::kCols; c += C::kLd) {
-                    uint32_t r[C::kLd];
-                    tmem_ld<C::kLd>(taddr + c, r);
-                    tmem_ld_wait();
-                    if (c + C::kLd == C::kCols) {
-                        // Last read of this buffer: hand it back to the MMA warp.
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(smem_u32(&tempty[b]));
+                for (int j = 0; j < C::kCols / 2; ++j)
+                    acc[j] = __ffma2_rn(as_float2(r[j]), uniform ? sc[0] : sc[j], acc[j]);
+                ++g;
+                return true;
+            };
+
+            if (!SWAP) {
+                // Four K blocks of scales per 16-byte load, the next four fetched
+                // while the current four are promoted.
+                auto sa4 = [&](int c) {   // this row's scales of K blocks c..c+3 (slot is [kb][row])
+                    return make_float4(sa_t[(c + 0) * kPRows], sa_t[(c + 1) * kPRows], sa_t[(c + 2) * kPRows],
+                                       sa_t[(c + 3) * kPRows]);
+                };
+                float4 a_cur = sa4(0);
+                float4 w_cur = *reinterpret_cast<const float4*>(sw_t);
+                for (int c = 0; c < KB && ok; c += 4) {
+                    float4 a_nxt = a_cur, w_nxt = w_cur;
+                    if (c + 4 < KB) {
+                        a_nxt = sa4(c + 4);
+                        w_nxt = *reinterpret_cast<const float4*>(sw_t + c + 4);
+                    }
+                    const float sk[4] = {a_cur.x * w_cur.x, a_cur.y * w_cur.y, a_cur.z * w_cur.z, a_cur.w * w_cur.w};
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        if (c + u >= KB) break;
+                        const float2 s2 = make_float2(sk[u], sk[u]);
+                        if (!promote(&s2, true)) {
+                            ok = false;
+                            break;
+                        }
+                    }
+                    a_cur = a_nxt;
+                    w_cur = w_nxt;
+                }
+            } else {
+                // The thread's kCols token scales of the next K block are fetched
+                // while the current one is promoted.
+                float4 a_cur[C::kScaleRegs], a_nxt[C::kScaleRegs];
+                float w_cur = sw_t[0], w_nxt = w_cur;
+#pragma unroll
+                for (int q = 0; q < C::kScaleRegs; ++q) a_cur[q] = reinterpret_cast<const float4*>(sa_t)[q];
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (kb + 1 < KB) {
+                        const float* nx = sa_t + (kb + 1) * C::kScaleCols;
+#pragma unroll
+                        for (int q = 0; q < C::kScaleRegs; ++q) a_nxt[q] = reinterpret_cast<const float4*>(nx)[q];
+                        w_nxt = sw_t[kb + 1];
+                    }
+                    float2 sc[C::kCols / 2];
+                    const float2 w2 = make_float2(w_cur, w_cur);
+#pragma unroll
+                    for (int q = 0; q < C::kScaleRegs; ++q) {
+                        sc[2 * q] = __fmul2_rn(make_float2(a_cur[q].x, a_cur[q].y), w2);
+                        sc[2 * q + 1] = __fmul2_rn(make_float2(a_cur[q].z, a_cur[q].w), w2);
+                    }
+                    if (!promote(sc, false)) {
+                        ok = false;
+                        break;
                     }
 #pragma unroll
-                    for (int j = 0; j < C::kLd; ++j) {
-                        const float sc = SWAP ? sq[kb * BN + col0 + c + j] : srow;
-                        acc[c + j] = fmaf(__uint_as_float(r[j]), sc, acc[c + j]);
-                    }
+                    for (int q = 0; q < C::kScaleRegs; ++q) a_cur[q] = a_nxt[q];
+                    w_cur = w_nxt;
                 }
             }
             if (!ok) break;
+            // This tile's scales are no longer read.
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&sempty[slot]));
 
             if (!SWAP) {
-                if (m_row < p.M) {
-                    __nv_bfloat16* dst = pr.out + static_cast<int64_t>(m_row) * pr.ldo + n0 + col0;
+                // bf16 block of this warp -> shared (64-byte swizzle: 16-byte
+                // chunk c of row r sits at chunk c ^ ((r >> 1) & 3)) -> one TMA store.
+                uint8_t* stg = out_stage + ew * C::kStageOutBytes;
+                if (lane == 0) bulk_wait_read_all();   // the previous tile's store has read the buffer
+                __syncwarp();
 #pragma unroll
-                    for (int c = 0; c < C::kCols; c += 8) {
-                        if (n0 + col0 + c < pr.N) {
-                            uint4 v;
-                            __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&v);
+                for (int c = 0; c < C::kCols / 8; ++c) {
+                    uint4 v;
+                    __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&v);
 #pragma unroll
-                            for (int i = 0; i < 4; ++i)
-                                h[i] = __floats2bfloat162_rn(acc[c + 2 * i], acc[c + 2 * i + 1]);
-                            *reinterpret_cast<uint4*>(dst + c) = v;
-                        }
-                    }
+                    for (int q = 0; q < 4; ++q) h[q] = __floats2bfloat162_rn(acc[4 * c + q].x, acc[4 * c + q].y);
+                    const int sc = c ^ ((lane >> 1) & 3);
+                    *reinterpret_cast<uint4*>(stg + lane * (C::kCols * 2) + sc * 16) = v;
+                }
+                fence_proxy_async_smem();              // generic-proxy writes -> visible to TMA
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_2d(pi ? &map_o1 : &map_o0, smem_u32(stg), n0 + col0, m0 + quarter * 32);
+                    bulk_commit();
                 }
             } else {
                 const int n = n0 + row;
@@ -491,13 +795,15 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
 #pragma unroll
                     for (int j = 0; j < C::kCols; ++j) {
                         const int m = m0 + col0 + j;
-                        if (m < p.M) pr.out[static_cast<int64_t>(m) * pr.ldo + n] = __float2bfloat16_rn(acc[j]);
+                        const float v = (j & 1) ? acc[j / 2].y : acc[j / 2].x;
+                        if (m < p.M) pr.out[static_cast<int64_t>(m) * pr.ldo + n] = __float2bfloat16_rn(v);
                     }
                 }
             }
         }
     }
 
+    if (!SWAP && warp >= 4 && lane == 0) bulk_wait_all();   // stores complete before the CTA exits
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
@@ -510,8 +816,10 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
 template <int BN, bool SWAP, int STAGES, int NBUF, int EPI_WARPS>
 constexpr size_t smem_bytes(int KB) {
     using C = Cfg<BN, SWAP, STAGES, NBUF, EPI_WARPS>;
-    return 1024 /* alignment slack */ + STAGES * C::kStageBytes + (2 * STAGES + 2 * NBUF + 1) * 8 + 16 +
-           (SWAP ? static_cast<size_t>(KB) * BN * 4 : 0);
+    const int KBP = (KB + 3) & ~3;
+    return 1024 /* alignment slack */ + STAGES * C::kStageBytes + EPI_WARPS * C::kStageOutBytes +
+           (2 * STAGES + 2 * NBUF + 5) * 8 + 16 + 16 +
+           static_cast<size_t>(2 * KBP * C::kScaleCols + 2 * KBP) * 4;
 }
 
 }  // namespace gemm
@@ -552,6 +860,21 @@ bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t K, int64_t
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D map over a bf16 output [rows, cols] with row stride ld elements; box =
+// 32 columns (64 bytes) x 32 rows, 64-byte swizzle (the staging layout of the
+// epilogue); stores past the extent are clipped.
+bool make_out_map(CUtensorMap* m, void* base, int64_t rows, int64_t cols, int64_t ld) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld * 2)};
+    cuuint32_t box[2] = {32, 32};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
 std::atomic<uint32_t> g_inject{0};
 std::atomic<uint64_t> g_timeout_ns{0};
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
@@ -580,7 +903,7 @@ dsnq_status check_consumer(const Consumer& c, int64_t K) {
 
 template <int BN, bool SWAP, int STAGES, int NBUF, int EPI_WARPS>
 dsnq_status launch(gemm::Params& prm, const CUtensorMap& ma, const CUtensorMap& mw0, const CUtensorMap& mw1,
-                   cudaStream_t stream) {
+                   const CUtensorMap& mo0, const CUtensorMap& mo1, cudaStream_t stream) {
     using C = gemm::Cfg<BN, SWAP, STAGES, NBUF, EPI_WARPS>;
     auto kern = gemm::block_scaled_gemm_kernel<BN, SWAP, STAGES, NBUF, EPI_WARPS>;
     const size_t smem = gemm::smem_bytes<BN, SWAP, STAGES, NBUF, EPI_WARPS>(prm.KB);
@@ -594,7 +917,7 @@ dsnq_status launch(gemm::Params& prm, const CUtensorMap& ma, const CUtensorMap& 
     // walking the tile space with a stride of the grid size.
     const int sms = device_sm_count();
     const int grid = prm.total_tiles < sms ? prm.total_tiles : (sms > 0 ? sms : prm.total_tiles);
-    kern<<<grid, C::kThreads, smem, stream>>>(ma, mw0, mw1, prm);
+    kern<<<grid, C::kThreads, smem, stream>>>(ma, mw0, mw1, mo0, mo1, prm);
     return launch_status();
 }
 
@@ -604,7 +927,7 @@ dsnq_status run_gemm(int64_t M, int64_t K, const void* a, int64_t lda, const flo
     if (M < 0 || K <= 0 || c0.N < 0 || c1.N < 0) return DSNQ_ERR_INVALID_ARG;
     if (layout != DSNQ_SCALE_ROW_MAJOR && layout != DSNQ_SCALE_COL_MAJOR) return DSNQ_ERR_INVALID_ARG;
     if (K % 128 != 0) return DSNQ_ERR_UNSUPPORTED;
-    if (M > 0x7fffffffLL || K > (1LL << 20)) return DSNQ_ERR_UNSUPPORTED;
+    if (M > 0x7fffffffLL || K > 8192) return DSNQ_ERR_UNSUPPORTED;
     if (M == 0) return DSNQ_OK;          // empty activations may come with NULL pointers
     if (!a || !as) return DSNQ_ERR_INVALID_ARG;
     if (lda < K) return DSNQ_ERR_INVALID_ARG;
@@ -632,10 +955,11 @@ dsnq_status run_gemm(int64_t M, int64_t K, const void* a, int64_t lda, const flo
     prm.a_scale = as;
     if (layout == DSNQ_SCALE_ROW_MAJOR) { prm.as_rs = ld; prm.as_gs = 1; }
     else { prm.as_rs = 1; prm.as_gs = ld; }
+    prm.vec_scales = layout == DSNQ_SCALE_COL_MAJOR && ld % 4 == 0 && aligned(as, 16);
     const int64_t rows_per_a_tile = swap ? bn : gemm::kPRows;
     prm.tiles_m = static_cast<int>((M + rows_per_a_tile - 1) / rows_per_a_tile);
 
-    CUtensorMap ma, mw[2];
+    CUtensorMap ma, mw[2], mo[2];
     if (!make_map(&ma, a, M, K, lda, a_box)) return DSNQ_ERR_CUDA;
     const Consumer* cs[2] = {&c0, &c1};
     int64_t total = 0;
@@ -652,12 +976,17 @@ dsnq_status run_gemm(int64_t M, int64_t K, const void* a, int64_t lda, const flo
         pr.out = static_cast<__nv_bfloat16*>(c.out);
         pr.ldo = c.ldo;
         if (!make_map(&mw[np], c.w, c.N, K, c.ldw, w_box)) return DSNQ_ERR_CUDA;
+        if (!swap && !make_out_map(&mo[np], c.out, M, c.N, c.ldo)) return DSNQ_ERR_CUDA;
         const int64_t tiles = static_cast<int64_t>(prm.tiles_m) * pr.tiles_n;
         if (np == 0) prm.tiles0 = static_cast<int>(tiles);
         total += tiles;
         ++np;
     }
-    if (np == 1) mw[1] = mw[0];
+    if (np == 1) {
+        mw[1] = mw[0];
+        mo[1] = mo[0];
+    }
+    if (swap) mo[0] = mo[1] = mw[0];   // unused by the decode variant
     if (total > 0x7fffffffLL) return DSNQ_ERR_UNSUPPORTED;
     prm.total_tiles = static_cast<int>(total);
     const uint64_t tmo = g_timeout_ns.load();
@@ -666,10 +995,15 @@ dsnq_status run_gemm(int64_t M, int64_t K, const void* a, int64_t lda, const flo
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     switch (bn) {
-        case 16: return launch<16, true, 8, 4, 8>(prm, ma, mw[0], mw[1], s);
-        case 32: return launch<32, true, 8, 4, 8>(prm, ma, mw[0], mw[1], s);
-        case 64: return launch<64, true, 8, 4, 8>(prm, ma, mw[0], mw[1], s);
-        default: return launch<128, false, 6, 4, 8>(prm, ma, mw[0], mw[1], s);
+        // Decode: the MMA per K block is tiny, so the MMA <-> promotion round
+        // trip sets the pace; a TMEM ring as deep as TMEM allows (512 / BN
+        // buffers) lets the MMA run a whole tile ahead of the promotion.
+        case 16: return launch<16, true, 8, 32, 8>(prm, ma, mw[0], mw[1], mo[0], mo[1], s);
+        case 32: return launch<32, true, 8, 16, 8>(prm, ma, mw[0], mw[1], mo[0], mo[1], s);
+        case 64: return launch<64, true, 8, 8, 8>(prm, ma, mw[0], mw[1], mo[0], mo[1], s);
+        default:
+            if (KB <= 16) return launch<128, false, 5, 4, 16>(prm, ma, mw[0], mw[1], mo[0], mo[1], s);
+            return launch<128, false, 3, 4, 16>(prm, ma, mw[0], mw[1], mo[0], mo[1], s);
     }
 }
 

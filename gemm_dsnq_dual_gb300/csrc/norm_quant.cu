@@ -35,8 +35,8 @@ namespace dsnq {
 
 constexpr int kThreads = 128;       // one warp-group per row
 constexpr int kChunk = 8;           // bf16 per 16-byte chunk
-// CTAs per SM the register budget is sized for (64 registers per thread up
-// to two chunks per thread, 128 beyond).
+// CTAs per SM the register budget of the warp-group-per-row kernel is sized
+// for (64 registers per thread up to two chunks per thread, 128 beyond).
 __host__ __device__ constexpr int min_blocks_per_sm(int passes) { return passes <= 2 ? 8 : 4; }
 constexpr float kE4M3Max = 448.0f;  // largest finite E4M3FN value
 
@@ -65,23 +65,10 @@ struct RowArgs {
     int64_t ldkv_out;
 };
 
-// ---- packed fp32 pairs (f32x2 instructions, sm_100+)
-__device__ __forceinline__ uint64_t as_u64(float2 v) {
-    return (static_cast<uint64_t>(__float_as_uint(v.y)) << 32) | __float_as_uint(v.x);
-}
-__device__ __forceinline__ float2 as_f2(uint64_t v) {
-    return make_float2(__uint_as_float(static_cast<uint32_t>(v)), __uint_as_float(static_cast<uint32_t>(v >> 32)));
-}
-__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
-    uint64_t d;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(as_u64(a)), "l"(as_u64(b)));
-    return as_f2(d);
-}
-__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
-    uint64_t d;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(as_u64(a)), "l"(as_u64(b)), "l"(as_u64(c)));
-    return as_f2(d);
-}
+// ---- packed fp32 pairs: the f32x2 arithmetic of sm_100+ through the CUDA
+// builtins (one instruction per pair).
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
 
 // Eight bf16 of a 16-byte chunk as four fp32 pairs (exact: bf16 is the top
 // half of an fp32).
@@ -99,28 +86,53 @@ __device__ __forceinline__ uint4 pack8_bf16(const float2 (&f)[4]) {
     return v;
 }
 
-// Quotient of the quantize step: the IEEE fp32 division x / scale, or a
-// signed zero for an all-zero group (scale == 0).
-__device__ __forceinline__ float quant_quotient(float x, float scale) {
-    return scale > 0.f ? __fdiv_rn(x, scale) : x * 0.f;
+// ---- the quantize step: code = e4m3_rn_satfinite(fp32(x / scale))
+//
+// The quotient is defined as the IEEE fp32 division x / scale.  Dividing
+// every element is expensive, so each group first forms y = fp32(1/scale)
+// (one correctly rounded reciprocal per group) and the approximation
+// q = fp32(x * y), whose relative distance to fp32(x / scale) is below 2^-22.
+// E4M3 rounding is monotone, so if q * (1 - 2^-20) and q * (1 + 2^-20) give
+// the same code, that code is the code of fp32(x / scale) too; otherwise (the
+// quotient sits within 2^-20 of an E4M3 rounding boundary, or the scale is
+// too small for its reciprocal to be finite) the pair takes the IEEE division.
+struct QuantScale {
+    float scale;   // amax / 448, IEEE fp32
+    float recip;   // fp32(1 / scale), 0 for an all-zero group
+    bool exact;    // true: always use the division (reciprocal not finite)
+};
+
+__device__ __forceinline__ QuantScale make_quant_scale(float amax) {
+    QuantScale qs;
+    qs.scale = amax / kE4M3Max;                       // IEEE fp32 divide
+    qs.exact = qs.scale > 0.f && qs.scale < 1.0e-36f;
+    qs.recip = (qs.scale > 0.f && !qs.exact) ? __frcp_rn(qs.scale) : 0.f;
+    return qs;
 }
 
-// Eight E4M3FN codes of x / scale, round-to-nearest-even with saturation to +-448.
-__device__ __forceinline__ uint2 pack8_e4m3(const float2 (&f)[4], float scale) {
-    uint32_t w[2];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        uint32_t word = 0;
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            const float2 x = f[2 * h + i];
-            const float2 q = make_float2(quant_quotient(x.x, scale), quant_quotient(x.y, scale));
-            const __nv_fp8x2_storage_t s = __nv_cvt_float2_to_fp8x2(q, __NV_SATFINITE, __NV_E4M3);
-            word |= static_cast<uint32_t>(s) << (16 * i);
-        }
-        w[h] = word;
-    }
-    return make_uint2(w[0], w[1]);
+__device__ __forceinline__ uint32_t e4m3x2(float2 v) {
+    return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(v, __NV_SATFINITE, __NV_E4M3));
+}
+
+// Four codes (little-endian bytes) of the values of the pairs v0, v1.
+__device__ __forceinline__ uint32_t quant4(float2 v0, float2 v1, const QuantScale& qs) {
+    const float2 y = make_float2(qs.recip, qs.recip);
+    const float2 q0 = mul2(v0, y), q1 = mul2(v1, y);
+    const float2 lo = make_float2(1.0f - 0x1p-20f, 1.0f - 0x1p-20f);
+    const float2 hi = make_float2(1.0f + 0x1p-20f, 1.0f + 0x1p-20f);
+    const uint32_t wlo = e4m3x2(mul2(q0, lo)) | (e4m3x2(mul2(q1, lo)) << 16);
+    const uint32_t whi = e4m3x2(mul2(q0, hi)) | (e4m3x2(mul2(q1, hi)) << 16);
+    if (wlo == whi && !qs.exact) return wlo;
+    if (qs.scale > 0.f)
+        return e4m3x2(make_float2(__fdiv_rn(v0.x, qs.scale), __fdiv_rn(v0.y, qs.scale))) |
+               (e4m3x2(make_float2(__fdiv_rn(v1.x, qs.scale), __fdiv_rn(v1.y, qs.scale))) << 16);
+    return e4m3x2(make_float2(v0.x * 0.f, v0.y * 0.f)) |           // all-zero group: signed zeros
+           (e4m3x2(make_float2(v1.x * 0.f, v1.y * 0.f)) << 16);
+}
+
+// Eight E4M3FN codes of x / scale (x as four pairs), little-endian in a uint2.
+__device__ __forceinline__ uint2 pack8_e4m3(const float2 (&f)[4], const QuantScale& qs) {
+    return make_uint2(quant4(f[0], f[1], qs), quant4(f[2], f[3], qs));
 }
 
 __device__ __forceinline__ float warp_sum(float v) {
@@ -234,10 +246,10 @@ row_norm_quant_kernel(const RowArgs a) {
             amax = half_warp_max(amax);
             if (!live[p]) continue;
             if (is_q[p]) {
-                const float scale = amax / kE4M3Max;      // IEEE fp32 divide
-                *reinterpret_cast<uint2*>(a.q_fp8 + m * a.ldq_out + col[p]) = pack8_e4m3(x[p], scale);
+                const QuantScale qs = make_quant_scale(amax);
+                *reinterpret_cast<uint2*>(a.q_fp8 + m * a.ldq_out + col[p]) = pack8_e4m3(x[p], qs);
                 if ((lane & 15) == 0)
-                    a.scale[m * a.scale_row_stride + (col[p] / 128) * a.scale_group_stride] = scale;
+                    a.scale[m * a.scale_row_stride + (col[p] / 128) * a.scale_group_stride] = qs.scale;
             } else if (MODE == kFused) {
                 *reinterpret_cast<uint4*>(a.kv_out + m * a.ldkv_out + col[p]) = pack8_bf16(x[p]);
             }
@@ -247,14 +259,158 @@ row_norm_quant_kernel(const RowArgs a) {
     }
 }
 
+// ---------------------------------------------------------------------------
+// One warp per token row, for rows of at most 256 chunks (DSv4: 192 q + 64
+// kv).  Lane l owns chunks l, l+32, ... (CPT of them); with Kq a multiple of
+// 128, each aligned half-warp of chunk slot j holds one q group.  No block
+// barrier per row: the row's sums of squares are warp shuffles.  Gamma lives
+// in shared memory as fp32, loaded once per CTA.
+// ---------------------------------------------------------------------------
+constexpr int kRowWarps = 4;        // rows in flight per CTA
+constexpr int kRowCtasPerSM = 3;    // register budget: up to 168 per thread
+
+template <int MODE, int CPT>
+__global__ void __launch_bounds__(kRowWarps * 32, kRowCtasPerSM)
+warp_row_kernel(const RowArgs a) {
+    extern __shared__ float gamma_s[];          // [Kq + Kkv] fp32
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int kq = a.cq * kChunk, width = (a.cq + a.ckv) * kChunk;
+
+    bool is_q[CPT], live[CPT];
+    int col[CPT];
+#pragma unroll
+    for (int j = 0; j < CPT; ++j) {
+        const int c = j * 32 + lane;
+        is_q[j] = c < a.cq;
+        live[j] = c < a.cq + a.ckv;
+        col[j] = (is_q[j] ? c : c - a.cq) * kChunk;
+    }
+
+    auto load_row = [&](int64_t m, uint4 (&raw)[CPT]) {
+#pragma unroll
+        for (int j = 0; j < CPT; ++j) {
+            raw[j] = make_uint4(0, 0, 0, 0);
+            if (live[j]) {
+                const __nv_bfloat16* src = is_q[j] ? a.q + m * a.ldq + col[j] : a.kv + m * a.ldkv + col[j];
+                raw[j] = __ldg(reinterpret_cast<const uint4*>(src));
+            }
+        }
+    };
+
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kRowWarps;
+    int64_t m = static_cast<int64_t>(blockIdx.x) * kRowWarps + warp;
+    uint4 cur[CPT];
+    if (m < a.M) load_row(m, cur);               // in flight while gamma is staged
+
+    if (MODE != kQuantOnly) {
+        for (int i = threadIdx.x * kChunk; i < width; i += kRowWarps * 32 * kChunk) {
+            const __nv_bfloat16* gsrc = i < kq ? a.gamma_q + i : a.gamma_kv + (i - kq);
+            float2 g[4];
+            unpack8(__ldg(reinterpret_cast<const uint4*>(gsrc)), g);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) reinterpret_cast<float2*>(gamma_s + i)[k] = g[k];
+        }
+        __syncthreads();
+    }
+
+    for (; m < a.M; m += stride) {
+        uint4 nxt[CPT];
+        const int64_t mn = m + stride;
+        if (mn < a.M) load_row(mn, nxt);         // prefetch this warp's next row
+
+        float2 x[CPT][4];
+#pragma unroll
+        for (int j = 0; j < CPT; ++j) unpack8(cur[j], x[j]);
+
+        if (MODE != kQuantOnly) {
+            float2 sq = make_float2(0.f, 0.f), skv = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int j = 0; j < CPT; ++j) {
+                float2 s2 = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) s2 = fma2(x[j][i], x[j][i], s2);
+                if (is_q[j]) { sq.x += s2.x; sq.y += s2.y; }    // dead chunks hold zeros
+                else { skv.x += s2.x; skv.y += s2.y; }
+            }
+            const float ssq_q = warp_sum(sq.x + sq.y);
+            const float ssq_kv = warp_sum(skv.x + skv.y);
+            // Correctly rounded sqrt and divide (not the approximate rsqrt).
+            const float r_q = 1.0f / sqrtf(ssq_q / a.kq_f + a.eps);
+            const float r_kv = 1.0f / sqrtf(ssq_kv / a.kkv_f + a.eps);
+#pragma unroll
+            for (int j = 0; j < CPT; ++j) {
+                const float r = is_q[j] ? r_q : r_kv;
+                const float2 r2 = make_float2(r, r);
+                const float4* gp = reinterpret_cast<const float4*>(gamma_s + (is_q[j] ? 0 : kq) + col[j]);
+                float4 g0 = make_float4(0.f, 0.f, 0.f, 0.f), g1 = g0;
+                if (live[j]) { g0 = gp[0]; g1 = gp[1]; }
+                x[j][0] = mul2(mul2(x[j][0], r2), make_float2(g0.x, g0.y));
+                x[j][1] = mul2(mul2(x[j][1], r2), make_float2(g0.z, g0.w));
+                x[j][2] = mul2(mul2(x[j][2], r2), make_float2(g1.x, g1.y));
+                x[j][3] = mul2(mul2(x[j][3], r2), make_float2(g1.z, g1.w));
+            }
+        }
+
+#pragma unroll
+        for (int j = 0; j < CPT; ++j) {
+            if (MODE == kNormOnly) {
+                if (!live[j]) continue;
+                if (is_q[j])
+                    *reinterpret_cast<uint4*>(a.q_bf16 + m * a.ldq_out + col[j]) = pack8_bf16(x[j]);
+                else
+                    *reinterpret_cast<uint4*>(a.kv_out + m * a.ldkv_out + col[j]) = pack8_bf16(x[j]);
+                continue;
+            }
+            float amax = 0.f;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) amax = fmaxf(amax, fmaxf(fabsf(x[j][i].x), fabsf(x[j][i].y)));
+            amax = half_warp_max(amax);
+            if (!live[j]) continue;
+            if (is_q[j]) {
+                const QuantScale qs = make_quant_scale(amax);
+                *reinterpret_cast<uint2*>(a.q_fp8 + m * a.ldq_out + col[j]) = pack8_e4m3(x[j], qs);
+                if ((lane & 15) == 0)
+                    a.scale[m * a.scale_row_stride + (col[j] / 128) * a.scale_group_stride] = qs.scale;
+            } else if (MODE == kFused) {
+                *reinterpret_cast<uint4*>(a.kv_out + m * a.ldkv_out + col[j]) = pack8_bf16(x[j]);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < CPT; ++j) cur[j] = nxt[j];
+    }
+}
+
 template <int MODE>
 static dsnq_status launch_rows(RowArgs a, int64_t M, cudaStream_t s) {
     const int chunks = a.cq + a.ckv;
     const int passes = (chunks + kThreads - 1) / kThreads;
     a.M = M;
-    // Enough CTAs to fill every SM at the register-limited occupancy; each
-    // walks its rows with a grid stride.
     const int sms = device_sm_count();
+    // Many rows: one warp per row (no block barrier per row).  Few rows: a
+    // warp-group per row, which shortens each thread's dependency chain.
+    const int64_t warp_row_min = sms > 0 ? static_cast<int64_t>(sms) * 8 : 2048;
+    if (chunks <= 8 * 32 && M >= warp_row_min) {
+        // Warp per row.  Enough CTAs to fill every SM at the register-limited occupancy.
+        const int cpt = (chunks + 31) / 32;
+        const int64_t rows_cap = sms > 0 ? static_cast<int64_t>(sms) * kRowCtasPerSM : (M + kRowWarps - 1) / kRowWarps;
+        const int64_t need = (M + kRowWarps - 1) / kRowWarps;
+        dim3 grid(static_cast<unsigned>(need < rows_cap ? need : rows_cap)), block(kRowWarps * 32);
+        const size_t smem = MODE == kQuantOnly ? 0 : static_cast<size_t>(chunks) * kChunk * sizeof(float);
+        switch (cpt) {
+            case 1: warp_row_kernel<MODE, 1><<<grid, block, smem, s>>>(a); break;
+            case 2: warp_row_kernel<MODE, 2><<<grid, block, smem, s>>>(a); break;
+            case 3: warp_row_kernel<MODE, 3><<<grid, block, smem, s>>>(a); break;
+            case 4: warp_row_kernel<MODE, 4><<<grid, block, smem, s>>>(a); break;
+            case 5: warp_row_kernel<MODE, 5><<<grid, block, smem, s>>>(a); break;
+            case 6: warp_row_kernel<MODE, 6><<<grid, block, smem, s>>>(a); break;
+            case 7: warp_row_kernel<MODE, 7><<<grid, block, smem, s>>>(a); break;
+            default: warp_row_kernel<MODE, 8><<<grid, block, smem, s>>>(a); break;
+        }
+        return launch_status();
+    }
+    // Wider rows: one warp-group per row.  Enough CTAs to fill every SM at the
+    // register-limited occupancy; each walks its rows with a grid stride.
     const int64_t cap = sms > 0 ? static_cast<int64_t>(sms) * min_blocks_per_sm(passes) : M;
     dim3 grid(static_cast<unsigned>(M < cap ? M : cap)), block(kThreads);
     switch (passes) {
@@ -297,8 +453,8 @@ weight_block_quant_kernel(int64_t N, int64_t K, const float* __restrict__ w, int
     amax = red[0];
 #pragma unroll
     for (int i = 1; i < 8; ++i) amax = fmaxf(amax, red[i]);
-    const float scale = amax / kE4M3Max;
-    if (t == 0) sw[nb * ldsw + kb] = scale;
+    const QuantScale qs = make_quant_scale(amax);
+    if (t == 0) sw[nb * ldsw + kb] = qs.scale;
     if (!live) return;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {  // 16 codes per 16-byte store
@@ -308,7 +464,7 @@ weight_block_quant_kernel(int64_t N, int64_t K, const float* __restrict__ w, int
             f0[i] = make_float2(v[16 * j + 2 * i], v[16 * j + 2 * i + 1]);
             f1[i] = make_float2(v[16 * j + 8 + 2 * i], v[16 * j + 8 + 2 * i + 1]);
         }
-        uint2 lo = pack8_e4m3(f0, scale), hi = pack8_e4m3(f1, scale);
+        uint2 lo = pack8_e4m3(f0, qs), hi = pack8_e4m3(f1, qs);
         *reinterpret_cast<uint4*>(out + row * ldo + c0 + 16 * j) = make_uint4(lo.x, lo.y, hi.x, hi.y);
     }
 }

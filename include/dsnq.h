@@ -204,7 +204,7 @@ DSNQ_API dsnq_status dsnq_quantize_weight_block128(
  *                ldw >= K, ldw % 16 == 0, 16-byte aligned.
  *   w_scale, ld_wscale : fp32 [ceil(N/128), K/128], ld_wscale >= K/128.
  *   out_bf16, ldo : bf16 [M, N], ldo >= N, ldo % 8 == 0, 16-byte aligned.
- * K must be a multiple of 128 (DSNQ_ERR_UNSUPPORTED otherwise) and N a
+ * K must be a multiple of 128 and at most 8192 (DSNQ_ERR_UNSUPPORTED otherwise) and N a
  * multiple of 16.  The output must not overlap the inputs.
  */
 DSNQ_API dsnq_status dsnq_block_scaled_fp8_gemm(
