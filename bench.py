@@ -53,6 +53,22 @@ def gemm_flops(M: int) -> float:
     return 2.0 * M * (N_ATTN + N_IDX) * KQ
 
 
+def captured_traffic(key: str):
+    """DRAM bytes per launch (read + write) from the committed ncu summary, or
+    None when the kernel's source has changed since the capture."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    rec = json.load(open(path)).get(key)
+    if not rec:
+        return None
+    src = os.path.join(ROOT, "gemm_dsnq_dual_gb300", "csrc", rec["source"])
+    if not os.path.exists(src) or hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] != rec["source_sha256_16"]:
+        return None
+    return rec["dram_bytes_per_launch"]
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -238,12 +254,17 @@ def run_ours(args, rank, world):
         },
         "roofline": {"bound": "tensor", "achieved": round(gemm_tflops, 1),
                      "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
-                     "frac": round(gemm_tflops / fp8_peak, 4), "traffic": None,
+                     "frac": round(gemm_tflops / fp8_peak, 4),
+                     "traffic": captured_traffic(f"gemm_dual_M{M}"),
+                     "algorithmic_bytes": int(M * (KQ + 4 * KQ // 128) + (N_ATTN + N_IDX) * KQ
+                                              + 2 * M * (N_ATTN + N_IDX)),
                      "kernel": "block_scaled_gemm_kernel (dual launch)",
                      "peak_source": f"{peak_src}: FP8 = 2 x bf16 dense burst ({bf16_tf} TFLOP/s)"},
         "roofline_norm_quant": {"bound": "hbm", "achieved": round(nq_gbs, 1), "peak": hbm_gbs,
                                 "unit": "GB/s", "frac": round(nq_gbs / hbm_gbs, 4),
-                                "traffic": None, "peak_source": peak_src},
+                                "traffic": captured_traffic(f"norm_quant_M{M}"),
+                                "algorithmic_bytes": M * NQ_BYTES_PER_ROW + NQ_BYTES_PER_CALL,
+                                "peak_source": peak_src},
         "wall_s_timed_region": round(t_wall, 3),
         "clocks": clocks,
     }

@@ -106,12 +106,23 @@ __device__ __forceinline__ QuantScale make_quant_scale(float amax) {
     QuantScale qs;
     qs.scale = amax / kE4M3Max;                       // IEEE fp32 divide
     qs.exact = qs.scale > 0.f && qs.scale < 1.0e-36f;
-    qs.recip = (qs.scale > 0.f && !qs.exact) ? __frcp_rn(qs.scale) : 0.f;
+    // The reciprocal only has to be within 2^-22 of 1/scale for the bracket
+    // below (relative width 2^-20), which the fast divide (2 ulp) meets.
+    qs.recip = (qs.scale > 0.f && !qs.exact) ? __fdividef(1.0f, qs.scale) : 0.f;
     return qs;
 }
 
 __device__ __forceinline__ uint32_t e4m3x2(float2 v) {
     return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(v, __NV_SATFINITE, __NV_E4M3));
+}
+
+// Exact path of quant4 (rare): the IEEE division itself.
+__device__ __noinline__ uint32_t quant4_exact(float2 v0, float2 v1, float scale) {
+    if (scale > 0.f)
+        return e4m3x2(make_float2(__fdiv_rn(v0.x, scale), __fdiv_rn(v0.y, scale))) |
+               (e4m3x2(make_float2(__fdiv_rn(v1.x, scale), __fdiv_rn(v1.y, scale))) << 16);
+    return e4m3x2(make_float2(v0.x * 0.f, v0.y * 0.f)) |           // all-zero group: signed zeros
+           (e4m3x2(make_float2(v1.x * 0.f, v1.y * 0.f)) << 16);
 }
 
 // Four codes (little-endian bytes) of the values of the pairs v0, v1.
@@ -123,11 +134,7 @@ __device__ __forceinline__ uint32_t quant4(float2 v0, float2 v1, const QuantScal
     const uint32_t wlo = e4m3x2(mul2(q0, lo)) | (e4m3x2(mul2(q1, lo)) << 16);
     const uint32_t whi = e4m3x2(mul2(q0, hi)) | (e4m3x2(mul2(q1, hi)) << 16);
     if (wlo == whi && !qs.exact) return wlo;
-    if (qs.scale > 0.f)
-        return e4m3x2(make_float2(__fdiv_rn(v0.x, qs.scale), __fdiv_rn(v0.y, qs.scale))) |
-               (e4m3x2(make_float2(__fdiv_rn(v1.x, qs.scale), __fdiv_rn(v1.y, qs.scale))) << 16);
-    return e4m3x2(make_float2(v0.x * 0.f, v0.y * 0.f)) |           // all-zero group: signed zeros
-           (e4m3x2(make_float2(v1.x * 0.f, v1.y * 0.f)) << 16);
+    return quant4_exact(v0, v1, qs.scale);
 }
 
 // Eight E4M3FN codes of x / scale (x as four pairs), little-endian in a uint2.
@@ -267,7 +274,7 @@ row_norm_quant_kernel(const RowArgs a) {
 // in shared memory as fp32, loaded once per CTA.
 // ---------------------------------------------------------------------------
 constexpr int kRowWarps = 4;        // rows in flight per CTA
-constexpr int kRowCtasPerSM = 3;    // register budget: up to 168 per thread
+constexpr int kRowCtasPerSM = 4;    // register budget: up to 128 per thread
 
 template <int MODE, int CPT>
 __global__ void __launch_bounds__(kRowWarps * 32, kRowCtasPerSM)
@@ -319,62 +326,67 @@ warp_row_kernel(const RowArgs a) {
         const int64_t mn = m + stride;
         if (mn < a.M) load_row(mn, nxt);         // prefetch this warp's next row
 
-        float2 x[CPT][4];
-#pragma unroll
-        for (int j = 0; j < CPT; ++j) unpack8(cur[j], x[j]);
-
+        // The row stays packed (bf16) in registers; it is unpacked once for
+        // the sums of squares and once more, chunk by chunk, for the outputs.
+        float r_q = 1.f, r_kv = 1.f;
         if (MODE != kQuantOnly) {
             float2 sq = make_float2(0.f, 0.f), skv = make_float2(0.f, 0.f);
 #pragma unroll
             for (int j = 0; j < CPT; ++j) {
+                float2 x[4];
+                unpack8(cur[j], x);
                 float2 s2 = make_float2(0.f, 0.f);
 #pragma unroll
-                for (int i = 0; i < 4; ++i) s2 = fma2(x[j][i], x[j][i], s2);
+                for (int i = 0; i < 4; ++i) s2 = fma2(x[i], x[i], s2);
                 if (is_q[j]) { sq.x += s2.x; sq.y += s2.y; }    // dead chunks hold zeros
                 else { skv.x += s2.x; skv.y += s2.y; }
             }
             const float ssq_q = warp_sum(sq.x + sq.y);
             const float ssq_kv = warp_sum(skv.x + skv.y);
             // Correctly rounded sqrt and divide (not the approximate rsqrt).
-            const float r_q = 1.0f / sqrtf(ssq_q / a.kq_f + a.eps);
-            const float r_kv = 1.0f / sqrtf(ssq_kv / a.kkv_f + a.eps);
+            r_q = 1.0f / sqrtf(ssq_q / a.kq_f + a.eps);
+            r_kv = 1.0f / sqrtf(ssq_kv / a.kkv_f + a.eps);
+        }
+
 #pragma unroll
-            for (int j = 0; j < CPT; ++j) {
+        for (int j = 0; j < CPT; ++j) {
+            float2 x[4];
+            unpack8(cur[j], x);
+            if (MODE != kQuantOnly) {
                 const float r = is_q[j] ? r_q : r_kv;
                 const float2 r2 = make_float2(r, r);
                 const float4* gp = reinterpret_cast<const float4*>(gamma_s + (is_q[j] ? 0 : kq) + col[j]);
                 float4 g0 = make_float4(0.f, 0.f, 0.f, 0.f), g1 = g0;
                 if (live[j]) { g0 = gp[0]; g1 = gp[1]; }
-                x[j][0] = mul2(mul2(x[j][0], r2), make_float2(g0.x, g0.y));
-                x[j][1] = mul2(mul2(x[j][1], r2), make_float2(g0.z, g0.w));
-                x[j][2] = mul2(mul2(x[j][2], r2), make_float2(g1.x, g1.y));
-                x[j][3] = mul2(mul2(x[j][3], r2), make_float2(g1.z, g1.w));
+                x[0] = mul2(mul2(x[0], r2), make_float2(g0.x, g0.y));
+                x[1] = mul2(mul2(x[1], r2), make_float2(g0.z, g0.w));
+                x[2] = mul2(mul2(x[2], r2), make_float2(g1.x, g1.y));
+                x[3] = mul2(mul2(x[3], r2), make_float2(g1.z, g1.w));
             }
-        }
-
-#pragma unroll
-        for (int j = 0; j < CPT; ++j) {
             if (MODE == kNormOnly) {
                 if (!live[j]) continue;
                 if (is_q[j])
-                    *reinterpret_cast<uint4*>(a.q_bf16 + m * a.ldq_out + col[j]) = pack8_bf16(x[j]);
+                    *reinterpret_cast<uint4*>(a.q_bf16 + m * a.ldq_out + col[j]) = pack8_bf16(x);
                 else
-                    *reinterpret_cast<uint4*>(a.kv_out + m * a.ldkv_out + col[j]) = pack8_bf16(x[j]);
+                    *reinterpret_cast<uint4*>(a.kv_out + m * a.ldkv_out + col[j]) = pack8_bf16(x);
                 continue;
             }
-            float amax = 0.f;
+            // Slots whose chunks are kv (or past the row) for the whole warp skip the group work.
+            if (__any_sync(0xffffffffu, is_q[j])) {
+                float amax = 0.f;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) amax = fmaxf(amax, fmaxf(fabsf(x[j][i].x), fabsf(x[j][i].y)));
-            amax = half_warp_max(amax);
-            if (!live[j]) continue;
-            if (is_q[j]) {
-                const QuantScale qs = make_quant_scale(amax);
-                *reinterpret_cast<uint2*>(a.q_fp8 + m * a.ldq_out + col[j]) = pack8_e4m3(x[j], qs);
-                if ((lane & 15) == 0)
-                    a.scale[m * a.scale_row_stride + (col[j] / 128) * a.scale_group_stride] = qs.scale;
-            } else if (MODE == kFused) {
-                *reinterpret_cast<uint4*>(a.kv_out + m * a.ldkv_out + col[j]) = pack8_bf16(x[j]);
+                for (int i = 0; i < 4; ++i) amax = fmaxf(amax, fmaxf(fabsf(x[i].x), fabsf(x[i].y)));
+                amax = half_warp_max(amax);
+                if (is_q[j]) {
+                    const QuantScale qs = make_quant_scale(amax);
+                    *reinterpret_cast<uint2*>(a.q_fp8 + m * a.ldq_out + col[j]) = pack8_e4m3(x, qs);
+                    if ((lane & 15) == 0)
+                        a.scale[m * a.scale_row_stride + (col[j] / 128) * a.scale_group_stride] = qs.scale;
+                    continue;
+                }
             }
+            if (MODE == kFused && live[j])
+                *reinterpret_cast<uint4*>(a.kv_out + m * a.ldkv_out + col[j]) = pack8_bf16(x);
         }
 #pragma unroll
         for (int j = 0; j < CPT; ++j) cur[j] = nxt[j];
