@@ -164,7 +164,7 @@ def run_ours(args, rank, world):
     fp8_peak = 2.0 * bf16_tf            # FP8 dense = 2x bf16 dense (nominal ratio)
 
     # ---- inputs and weights, resident in HBM (weights quantized on the GPU at load time)
-    lat = inputs.full_path_batch(M, seed=3 + rank)
+    lat = inputs.full_path_batch(M, seed=rank_seed(rank))
     q, kv = lat.q.to(dev), lat.kv.to(dev)
     gq, gkv = lat.gamma_q.to(dev), lat.gamma_kv.to(dev)
     wa, swa = dsnq.quantize_weight_block128(inputs.weight(N_ATTN, KQ, seed=0, salt=1).to(dev))
@@ -226,7 +226,7 @@ def run_ours(args, rank, world):
     nq_avg, gm_avg = sum(nq_ms) / K, sum(gm_ms) / K
     gemm_tflops = gemm_flops(M) / (gm_avg * 1e-3) / 1e12
     nq_gbs = (M * NQ_BYTES_PER_ROW + NQ_BYTES_PER_CALL) / (nq_avg * 1e-3) / 1e9
-    value = world * gemm_flops(M) / (step_ms_max * 1e-3) / 1e12
+    value = whole_job_value(world, gemm_flops(M), step_ms_max)
     line = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -520,6 +520,18 @@ def run_reference(args, rank, world):
 
 
 # ----------------------------------------------------------------- plumbing
+
+def rank_seed(rank: int) -> int:
+    """Seed of the token batch a rank processes: ranks shard the work by
+    taking independent batches (weak scaling, no data exchange)."""
+    return 3 + rank
+
+
+def whole_job_value(world: int, flops_per_rank_step: float, step_ms_max: float) -> float:
+    """TFLOP/s of the whole job: the work of all ranks over the slowest
+    rank's step time."""
+    return world * flops_per_rank_step / (step_ms_max * 1e-3) / 1e12
+
 
 def barrier(world):
     if world > 1:

@@ -17,17 +17,18 @@
 //   * One pipeline stage is one 128-wide K block, i.e. exactly one scale
 //     block.  The activation scale differs per row and per K block, so it
 //     cannot be folded into the MMA: each K block is accumulated from zero into
-//     one of two TMEM buffers, and the promotion warps read it back
-//     (tcgen05.ld), multiply by sa * sw and add it into fp32 registers while the
-//     MMA of the next K block fills the other buffer.
+//     one of NBUF TMEM buffers, and the promotion warps read it back
+//     (tcgen05.ld), multiply by sa * sw and add it into fp32 registers while
+//     the MMAs of the next K blocks fill the other buffers.
 //   * Warp roles: warp 0 issues TMA, warp 1 allocates TMEM and issues MMA
-//     (one lane), warp 2 is the gate, warps 4.. promote and store.  Any wait
-//     or shared-memory load in the thread that issues tcgen05.mma stalls it
-//     behind the MMAs already in flight (about one K block per wait, measured
-//     on GB300), so the MMA thread performs none in steady state: the gate
-//     thread waits for "stage loaded" and "TMEM buffer free" and publishes a
-//     running count of K blocks ready, which the MMA thread re-reads only when
-//     it has caught up with its last reading.  Warp w may only read TMEM lanes
+//     (the whole warp runs the loop, one elected lane issues), warp 2 is the
+//     gate, warp 3 loads the scales, warps 4.. promote and store.  A wait or
+//     shared-memory load in the MMA-issuing warp stalls it behind the MMAs
+//     already in flight (about 100 cycles each, measured on GB300), so the
+//     MMA warp performs almost none: the gate thread waits for "stage loaded"
+//     and "TMEM buffer free" and publishes a running count of K blocks ready,
+//     which the MMA warp re-reads only when it has caught up with its last
+//     reading.  Warp w may only read TMEM lanes
 //     32*(w%4)..+31, so each group of four promotion warps covers all 128 lanes
 //     and the groups split the tile's columns.
 //   * Orientation.  The MMA's M side ("P", 128 rows) and N side ("Q", BN rows)
@@ -234,18 +235,26 @@ __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
+// The MMA-issuing code runs converged in a whole warp (warp-uniform values,
+// so they can live in uniform registers); one elected lane issues each
+// tcgen05 instruction.  Issuing from a divergent single lane measured about
+// 1.5x slower per K block on GB300.
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-                 : "memory");
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
+        : "memory");
 }
 
-// D[tmem] (+)= A[smem] * B[smem]^T, E4M3 x E4M3 -> fp32.
+// D[tmem] (+)= A[smem] * B[smem]^T, E4M3 x E4M3 -> fp32 (elected lane).
 __device__ __forceinline__ void tc_mma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                           uint32_t idesc, uint32_t accumulate) {
     asm volatile(
-        "{\n\t.reg .pred p;\n\t"
+        "{\n\t.reg .pred p, e;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
@@ -553,9 +562,9 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
             }
         }
     } else if (warp == 1) {
-        // ------------------------------------------------ MMA issuer (one lane)
+        // ------------------------------------------------ MMA issuer (whole warp, elected lane)
         constexpr uint32_t idesc = idesc_e4m3(BN);
-        if (lane == 0) {
+        {
             // Descriptors of stage 0; stage s and K slice k only move the start
             // address field (16-byte units), which stays below 2^14 for 227 KB.
             const uint64_t dp0 = smem_desc_k_sw128(smem_u32(tiles));
