@@ -77,6 +77,9 @@ struct Params {
     int tiles_m;                   // tiles along the activation rows
     int tiles0;                    // tiles of problem 0
     int total_tiles;               // tiles of both problems
+    int tiles_m2;                  // CTA-pair kernel: 256-row tiles along the activations
+    int super0;                    // CTA-pair kernel: 256 x 256 tiles of problem 0
+    int total_super;               // CTA-pair kernel: 256 x 256 tiles of both problems
     int vec_scales;                // column-major scales whose columns are 16-byte aligned
     Problem prob[2];
     uint64_t timeout_ns;
@@ -831,6 +834,448 @@ constexpr size_t smem_bytes(int KB) {
            static_cast<size_t>(2 * KBP * C::kScaleCols + 2 * KBP) * 4;
 }
 
+// ------------------------------------------------------------ CTA-pair kernel
+//
+// Large M.  A cluster of two CTAs on two SMs computes a 256 x 256 output tile
+// with tcgen05.mma.cta_group::2 (MMA shape M=256, N=256).  CTA r (cluster
+// rank r) holds activation rows 128r..128r+127 and weight rows 128r..128r+127
+// of the tile in its own shared memory; the even CTA issues the MMAs, which
+// read both CTAs' operands and leave each CTA's 128 x 256 fp32 partial sum in
+// that CTA's TMEM.  Per SM and K block this lands 32 KB of operands for twice
+// the MMA work of a 128 x 128 tile: on GB300 one SM takes in about 80-115 B
+// per clock from L2 under load (measured), less than the 128 B/clock that
+// 128 x 128 tiles need at the full MMA rate, and more than the 64 B/clock
+// these tiles need.
+//
+// Roles as in block_scaled_gemm_kernel; the MMA warp and the gate run in the
+// even CTA only.  Both CTAs' loads signal the even CTA's stage barrier
+// (TMA .cta_group::2); the MMA completions are multicast to both CTAs'
+// "stage free" and "partial ready" barriers; both CTAs' promotion warps
+// release a TMEM buffer on the even CTA's barrier.  Each promotion thread
+// carries 64 fp32 accumulators, so the role warps give up registers
+// (setmaxnreg) to the promotion warps.
+namespace pair {
+constexpr int kBN = 256;                        // output columns of a tile (both CTAs)
+constexpr int kStages = 5;
+constexpr int kNBuf = 2;                        // TMEM partial buffers of 256 columns
+constexpr int kEpiWarps = 16;
+constexpr int kThreads = (4 + kEpiWarps) * 32;
+constexpr int kHalfBytes = kPRows * kBK;        // 16 KB: 128 rows x 128 K bytes
+constexpr int kStageBytes = 2 * kHalfBytes;     // this CTA's activation rows + weight rows
+constexpr int kCols = 64;                       // accumulator columns per promotion thread
+constexpr int kLdCols = 16;                     // columns per TMEM load
+constexpr int kStageOutBytes = 32 * 32 * 2;     // one 32 x 32 bf16 block per promotion warp
+constexpr int kTmemCols = 512;
+constexpr uint32_t kRegsLaunch = 96;            // 65536 / 640, in steps of 8
+constexpr uint32_t kRegsRole = 56;
+constexpr uint32_t kRegsEpi = 104;
+static_assert(4 * 32 * kRegsRole + kEpiWarps * 32 * kRegsEpi <= kThreads * kRegsLaunch,
+              "the register split must fit in what the block is launched with");
+static_assert(kNBuf * kBN <= kTmemCols, "TMEM holds 512 fp32 columns");
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_id_x() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_count_x() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+    return r;
+}
+// All threads of both CTAs arrive, then wait for all.
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Address of the same shared-memory location in the CTA of cluster rank `rank`.
+__device__ __forceinline__ uint32_t peer_addr(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+// Arrival on a barrier of the peer CTA.  Relaxed: the only thing it reports
+// is that this warp's TMEM loads have completed (tcgen05.wait::ld), which
+// needs no release of earlier memory operations; a release at cluster scope
+// measured ~1000 cycles per arrival on GB300.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+// Tiled load into this CTA's shared memory whose completion is counted on a
+// barrier of this CTA or of its peer (cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar_cluster,
+                                                 int32_t x, int32_t y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.cta_group::2"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y)
+        : "memory");
+}
+__device__ __forceinline__ void tc_mma_f8_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                               uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Arrive on the barrier at offset `bar` of both CTAs once the MMAs issued so
+// far have completed.
+__device__ __forceinline__ void tc_commit_pair_both(uint32_t bar) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n\t}"
+        ::"r"(bar), "h"(static_cast<uint16_t>(0x3))
+        : "memory");
+}
+__device__ __forceinline__ void tc_commit_pair_local(uint32_t bar) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
+        : "memory");
+}
+// Instruction descriptor: D fp32, A and B E4M3, K-major, M = 256, N = 256.
+__host__ __device__ constexpr uint32_t idesc_e4m3_pair() {
+    return (1u << 4) | (static_cast<uint32_t>(kBN >> 3) << 17) | (static_cast<uint32_t>(256 >> 4) << 24);
+}
+
+constexpr size_t smem_bytes(int KB) {
+    const int KBP = (KB + 3) & ~3;
+    return 1024 + kStages * kStageBytes + kEpiWarps * kStageOutBytes + (2 * kStages + 2 * kNBuf + 5) * 8 + 32 +
+           static_cast<size_t>(2 * KBP * kPRows + 2 * 2 * KBP) * 4;
+}
+}  // namespace pair
+
+__global__ void __launch_bounds__(pair::kThreads, 1)
+pair_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_w0,
+                 const __grid_constant__ CUtensorMap map_w1, const __grid_constant__ CUtensorMap map_o0,
+                 const __grid_constant__ CUtensorMap map_o1, const Params p) {
+    using namespace pair;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* tiles = smem;
+    uint8_t* out_stage = smem + kStages * kStageBytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(out_stage + kEpiWarps * kStageOutBytes);
+    uint64_t* full = bars;                    // [S]  even CTA: both CTAs' loads of a stage
+    uint64_t* empty = bars + kStages;         // [S]  MMA -> TMA (multicast to both)
+    uint64_t* tfull = bars + 2 * kStages;     // [NB] MMA -> promotion (multicast to both)
+    uint64_t* tempty = tfull + kNBuf;         // [NB] even CTA: both CTAs' promotion -> gate
+    uint64_t* sfull = tempty + kNBuf;         // [2]
+    uint64_t* sempty = sfull + 2;             // [2]
+    uint64_t* drain = sempty + 2;             // [1]
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+    uint32_t* gate = tmem_holder + 2;
+    const int KBP = (p.KB + 3) & ~3;
+    float* sa_slots = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(tmem_holder + 8) + 15) & ~uintptr_t(15));
+    float* sw_slots = sa_slots + 2 * KBP * kPRows;     // [2][2 blocks][KBP]
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool even = rank == 0;
+    const int first = static_cast<int>(cluster_id_x()), stride = static_cast<int>(cluster_count_x());
+    const int items = first < p.total_super ? (p.total_super - 1 - first) / stride + 1 : 0;
+    const int KB = p.KB;
+
+    // Tile t -> problem, first activation row of this CTA, first output column.
+    auto coords = [&](int t, int& pi, int& m0, int& n0) {
+        pi = t < p.super0 ? 0 : 1;
+        if (pi) t -= p.super0;
+        m0 = (t % p.tiles_m2) * 256 + static_cast<int>(rank) * kPRows;
+        n0 = (t / p.tiles_m2) * kBN;
+    };
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(smem_u32(&full[s]), 1);
+            mbar_init(smem_u32(&empty[s]), 1);
+        }
+        for (int b = 0; b < kNBuf; ++b) {
+            mbar_init(smem_u32(&tfull[b]), 1);
+            mbar_init(smem_u32(&tempty[b]), 2 * kEpiWarps);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_u32(&sfull[i]), 32);
+            mbar_init(smem_u32(&sempty[i]), kEpiWarps);
+        }
+        mbar_init(smem_u32(drain), 1);
+        *abort_flag = 0;
+        *gate = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        tma_prefetch_desc(&map_a);
+        tma_prefetch_desc(&map_w0);
+        tma_prefetch_desc(&map_w1);
+        tma_prefetch_desc(&map_o0);
+        tma_prefetch_desc(&map_o1);
+    }
+    if (warp == 1) {
+        // One warp of each CTA of the pair allocates, collectively.
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_holder)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();          // both CTAs' barriers exist before any load or arrival targets them
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+    const uint64_t tmo = p.timeout_ns;
+
+    // Warp-group 0 (the role warps) hands registers to the promotion warps.
+    if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsRole));
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer (2*S lanes, both CTAs)
+        if (lane < 2 * kStages) {
+            const uint32_t ng = static_cast<uint32_t>(items) * KB;
+            const int s = lane >> 1;
+            const bool loads_w = lane & 1;
+            const uint32_t fb = peer_addr(smem_u32(&full[s]), 0);   // the even CTA's stage barrier
+            uint8_t* st = tiles + s * kStageBytes;
+            uint32_t last = 0;
+            bool ok = true;
+            for (uint32_t g = s; g < ng; g += kStages) {
+                if (!wait_bounded(smem_u32(&empty[s]), ((g / kStages) & 1) ^ 1, abort_flag, tmo)) {
+                    ok = false;
+                    break;
+                }
+                if ((p.inject & 1u) && g == 0) continue;   // test hook: never arrive on full[0]
+                const int tl = static_cast<int>(g / KB), kb = static_cast<int>(g % KB);
+                int pi, m0, n0;
+                coords(first + tl * stride, pi, m0, n0);
+                if (!loads_w) {
+                    if (even) mbar_arrive_expect_tx(smem_u32(&full[s]), 2 * kStageBytes);
+                    tma_load_2d_pair(smem_u32(st), &map_a, fb, kb * kBK, m0);
+                } else {
+                    tma_load_2d_pair(smem_u32(st + kHalfBytes), pi ? &map_w1 : &map_w0, fb, kb * kBK,
+                                     n0 + static_cast<int>(rank) * kPRows);
+                }
+                last = g + 1;
+            }
+            if (ok && last > 0) {
+                // Tail: the stage is released once the MMAs have read this lane's
+                // last copy, i.e. once the last arrival aimed at this CTA has landed.
+                const uint32_t gn = last - 1 + kStages;
+                ok = wait_bounded(smem_u32(&empty[s]), ((gn / kStages) & 1) ^ 1, abort_flag, tmo);
+            }
+            (void)ok;
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer (even CTA, whole warp)
+        if (even) {
+            constexpr uint32_t idesc = idesc_e4m3_pair();
+            const uint64_t da0 = smem_desc_k_sw128(smem_u32(tiles));
+            const uint64_t dw0 = smem_desc_k_sw128(smem_u32(tiles + kHalfBytes));
+            uint32_t g = 0, ready = 0;
+            bool ok = true, any = false;
+            for (int it = 0; it < items && ok; ++it) {
+                for (int kb = 0; kb < KB; ++kb, ++g) {
+                    const int s = g % kStages;
+                    const int b = g % kNBuf;
+                    if (g >= ready && !wait_gate(smem_u32(gate), g, ready, abort_flag, tmo)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t so = static_cast<uint64_t>((s * kStageBytes) >> 4);
+                    const uint32_t d = tmem_base + static_cast<uint32_t>(b * kBN);
+#pragma unroll
+                    for (int k = 0; k < kBK / kUmmaK; ++k) {
+                        const uint64_t ko = so + static_cast<uint64_t>((k * kUmmaK) >> 4);
+                        tc_mma_f8_pair(d, da0 + ko, dw0 + ko, idesc, k > 0 ? 1u : 0u);
+                    }
+                    tc_commit_pair_both(smem_u32(&empty[s]));
+                    tc_commit_pair_both(smem_u32(&tfull[b]));
+                    any = true;
+                }
+            }
+            if (*abort_flag && any) {
+                tc_commit_pair_local(smem_u32(drain));
+                wait_drain(smem_u32(drain), 0, tmo);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 2) {
+        // ------------------------------------------------ gate (even CTA, one lane)
+        if (even && lane == 0) {
+            uint32_t g = 0;
+            bool ok = true;
+            for (int it = 0; it < items && ok; ++it) {
+                for (int kb = 0; kb < KB; ++kb, ++g) {
+                    if (!wait_bounded<true>(smem_u32(&full[g % kStages]), (g / kStages) & 1, abort_flag, tmo) ||
+                        !wait_bounded<true>(smem_u32(&tempty[g % kNBuf]), ((g / kNBuf) & 1) ^ 1, abort_flag, tmo)) {
+                        ok = false;
+                        break;
+                    }
+                    st_release_shared(smem_u32(gate), g + 1);
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 3) {
+        // ------------------------------------------------ scale loader (whole warp, both CTAs)
+        for (int i = 0; i < items; ++i) {
+            const int slot = i & 1;
+            const bool got = wait_bounded(smem_u32(&sempty[slot]), ((i >> 1) & 1) ^ 1, abort_flag, tmo);
+            if (!__all_sync(0xffffffffu, got)) break;
+            int pi, m0, n0;
+            coords(first + i * stride, pi, m0, n0);
+            const Problem pr = pi ? p.prob[1] : p.prob[0];
+            float* sa_dst = sa_slots + slot * KBP * kPRows;     // [kb][128 rows]
+            const int rows = p.M - m0;
+            if (p.vec_scales && rows >= kPRows) {
+                for (int e = lane; e < KB * (kPRows / 4); e += 32) {
+                    const int kb = e / (kPRows / 4), v = e % (kPRows / 4);
+                    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(sa_dst + kb * kPRows + 4 * v)),
+                                 "l"(p.a_scale + static_cast<int64_t>(kb) * p.as_gs + m0 + 4 * v)
+                                 : "memory");
+                }
+            } else {
+                for (int e = lane; e < KB * kPRows; e += 32) {
+                    const int kb = e / kPRows, j = e % kPRows;
+                    const int m = m0 + j;
+                    const bool live = m < p.M;
+                    const float* src = live ? p.a_scale + static_cast<int64_t>(m) * p.as_rs + kb * p.as_gs : p.a_scale;
+                    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(sa_dst + e)), "l"(src),
+                                 "r"(live ? 4 : 0)
+                                 : "memory");
+                }
+            }
+            // The tile's two 128-feature weight-scale blocks (a block past the
+            // end, whose features are not stored, repeats the last one).
+            const int nblocks = (pr.N + kPRows - 1) / kPRows;
+            for (int e = lane; e < 2 * KB; e += 32) {
+                const int h = e / KB, kb = e % KB;
+                int nb = n0 / kPRows + h;
+                nb = nb < nblocks ? nb : nblocks - 1;
+                asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(sw_slots + (slot * 2 + h) * KBP + kb)),
+                             "l"(pr.w_scale + static_cast<int64_t>(nb) * pr.ld_ws + kb)
+                             : "memory");
+            }
+            asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(&sfull[slot])) : "memory");
+        }
+        asm volatile("cp.async.wait_all;" ::: "memory");
+    }
+    } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsEpi));
+        // ------------------------------------------------ promotion + store (both CTAs)
+        const int ew = warp - 4;
+        const int quarter = warp & 3;            // TMEM lanes 32*quarter .. +31
+        const int slice = ew >> 2;               // columns 64*slice .. +63 of the tile
+        const int row = quarter * 32 + lane;
+        const int col0 = slice * kCols;
+        static_assert(kNBuf == 2, "two buffer-free barriers in the even CTA");
+        const uint32_t tempty_even0 = peer_addr(smem_u32(&tempty[0]), 0);
+        const uint32_t tempty_even1 = peer_addr(smem_u32(&tempty[1]), 0);
+        uint32_t g = 0;
+        bool ok = true;
+        for (int i = 0; i < items && ok; ++i) {
+            int pi, m0, n0;
+            coords(first + i * stride, pi, m0, n0);
+            const Problem pr = pi ? p.prob[1] : p.prob[0];
+            const int slot = i & 1;
+            {
+                const bool got = wait_bounded(smem_u32(&sfull[slot]), (i >> 1) & 1, abort_flag, tmo);
+                if (!__all_sync(0xffffffffu, got)) break;
+            }
+            const float* sa_t = sa_slots + slot * KBP * kPRows + row;
+            const float* sw_t = sw_slots + (slot * 2 + (slice >> 1)) * KBP;
+
+            float2 acc[kCols / 2];
+#pragma unroll
+            for (int j = 0; j < kCols / 2; ++j) acc[j] = make_float2(0.f, 0.f);
+
+            float a_nxt = sa_t[0], w_nxt = sw_t[0];
+            for (int kb = 0; kb < KB; ++kb) {
+                const float sk = a_nxt * w_nxt;
+                if (kb + 1 < KB) {
+                    a_nxt = sa_t[(kb + 1) * kPRows];
+                    w_nxt = sw_t[kb + 1];
+                }
+                const int b = g % kNBuf;
+                const bool got = wait_bounded<true>(smem_u32(&tfull[b]), (g / kNBuf) & 1, abort_flag, tmo);
+                if (!__all_sync(0xffffffffu, got)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const float2 s2 = make_float2(sk, sk);
+                const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                       static_cast<uint32_t>(b * kBN + col0);
+#pragma unroll
+                for (int h = 0; h < kCols / kLdCols; ++h) {
+                    uint64_t r[kLdCols / 2];
+                    tmem_ld_pairs<kLdCols>(tbase + h * kLdCols, r);
+#pragma unroll
+                    for (int j = 0; j < kLdCols / 2; ++j)
+                        acc[h * (kLdCols / 2) + j] = __ffma2_rn(as_float2(r[j]), s2, acc[h * (kLdCols / 2) + j]);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    if (even)
+                        mbar_arrive(smem_u32(&tempty[b]));
+                    else
+                        mbar_arrive_remote(b ? tempty_even1 : tempty_even0);
+                }
+                ++g;
+            }
+            if (!ok) break;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&sempty[slot]));
+
+            // Epilogue: this warp's 32 rows x 64 columns, as two 32 x 32 bf16
+            // blocks through one 64-byte-swizzled staging buffer.
+            uint8_t* stg = out_stage + ew * kStageOutBytes;
+            const int r0 = m0 + quarter * 32;
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                const int c0 = n0 + col0 + half * 32;
+                if (lane == 0) bulk_wait_read_all();
+                __syncwarp();
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint4 v;
+                    __nv_bfloat162* hv = reinterpret_cast<__nv_bfloat162*>(&v);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const float2 a = acc[half * 16 + 4 * c + q];
+                        hv[q] = __floats2bfloat162_rn(a.x, a.y);
+                    }
+                    const int sc = c ^ ((lane >> 1) & 3);
+                    *reinterpret_cast<uint4*>(stg + lane * 64 + sc * 16) = v;
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0 && r0 < p.M && c0 < pr.N) {
+                    tma_store_2d(pi ? &map_o1 : &map_o0, smem_u32(stg), c0, r0);
+                    bulk_commit();
+                }
+            }
+        }
+    }
+
+    if (warp >= 4 && lane == 0) bulk_wait_all();
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();          // no CTA leaves while its peer may still address its memory
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kTmemCols)
+                     : "memory");
+    }
+}
+
 }  // namespace gemm
 
 // --------------------------------------------------------------------- host
@@ -930,6 +1375,49 @@ dsnq_status launch(gemm::Params& prm, const CUtensorMap& ma, const CUtensorMap& 
     return launch_status();
 }
 
+// CTA-pair kernel: as many 2-CTA clusters as fit at once, each walking the
+// 256 x 256 tiles with a stride of the cluster count.
+dsnq_status launch_pair(gemm::Params& prm, const CUtensorMap& ma, const CUtensorMap& mw0, const CUtensorMap& mw1,
+                        const CUtensorMap& mo0, const CUtensorMap& mo1, cudaStream_t stream) {
+    const size_t smem = gemm::pair::smem_bytes(prm.KB);
+    if (smem > 227 * 1024) return DSNQ_ERR_UNSUPPORTED;
+    auto kern = gemm::pair_gemm_kernel;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return DSNQ_ERR_CUDA;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(gemm::pair::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    static std::atomic<int> fit{-1};     // clusters resident at once
+    int clusters = fit.load();
+    if (clusters < 0) {
+        cfg.gridDim = dim3(2 * 128, 1, 1);
+        if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) != cudaSuccess) {
+            cudaGetLastError();
+            return DSNQ_ERR_CUDA;
+        }
+        fit.store(clusters);
+    }
+    if (clusters <= 0) return DSNQ_ERR_UNSUPPORTED;
+    const int n = prm.total_super < clusters ? prm.total_super : clusters;
+    cfg.gridDim = dim3(2 * n, 1, 1);
+    if (cudaLaunchKernelEx(&cfg, kern, ma, mw0, mw1, mo0, mo1, prm) != cudaSuccess) {
+        cudaGetLastError();
+        return DSNQ_ERR_CUDA;
+    }
+    return DSNQ_OK;
+}
+
 dsnq_status run_gemm(int64_t M, int64_t K, const void* a, int64_t lda, const float* as,
                      dsnq_scale_layout layout, int64_t ld_as, const Consumer& c0, const Consumer& c1,
                      void* stream) {
@@ -950,9 +1438,11 @@ dsnq_status run_gemm(int64_t M, int64_t K, const void* a, int64_t lda, const flo
     if (st != DSNQ_OK) return st;
     if (c0.N == 0 && c1.N == 0) return DSNQ_OK;
 
-    // Decode batches (M <= 64): swap-AB, the tokens are the MMA's N.
-    // Otherwise 128x128 tiles with four TMEM partial buffers.
+    // Decode batches (M <= 64): swap-AB, the tokens are the MMA's N.  From
+    // 256 rows on, 256 x 256 tiles on CTA pairs; in between 128x128 tiles
+    // with four TMEM partial buffers.
     const bool swap = M <= 64;
+    const bool paired = !swap && M >= 256;
     const int bn = swap ? (M <= 16 ? 16 : M <= 32 ? 32 : 64) : 128;
     const int a_box = swap ? bn : gemm::kPRows;
     const int w_box = swap ? gemm::kPRows : bn;
@@ -971,8 +1461,9 @@ dsnq_status run_gemm(int64_t M, int64_t K, const void* a, int64_t lda, const flo
     CUtensorMap ma, mw[2], mo[2];
     if (!make_map(&ma, a, M, K, lda, a_box)) return DSNQ_ERR_CUDA;
     const Consumer* cs[2] = {&c0, &c1};
-    int64_t total = 0;
+    int64_t total = 0, total_super = 0;
     int np = 0;
+    prm.tiles_m2 = static_cast<int>((M + 255) / 256);
     for (int i = 0; i < 2; ++i) {
         const Consumer& c = *cs[i];
         if (c.N == 0) continue;
@@ -987,8 +1478,13 @@ dsnq_status run_gemm(int64_t M, int64_t K, const void* a, int64_t lda, const flo
         if (!make_map(&mw[np], c.w, c.N, K, c.ldw, w_box)) return DSNQ_ERR_CUDA;
         if (!swap && !make_out_map(&mo[np], c.out, M, c.N, c.ldo)) return DSNQ_ERR_CUDA;
         const int64_t tiles = static_cast<int64_t>(prm.tiles_m) * pr.tiles_n;
-        if (np == 0) prm.tiles0 = static_cast<int>(tiles);
+        const int64_t supers = static_cast<int64_t>(prm.tiles_m2) * ((c.N + 255) / 256);
+        if (np == 0) {
+            prm.tiles0 = static_cast<int>(tiles);
+            prm.super0 = static_cast<int>(supers);
+        }
         total += tiles;
+        total_super += supers;
         ++np;
     }
     if (np == 1) {
@@ -998,11 +1494,13 @@ dsnq_status run_gemm(int64_t M, int64_t K, const void* a, int64_t lda, const flo
     if (swap) mo[0] = mo[1] = mw[0];   // unused by the decode variant
     if (total > 0x7fffffffLL) return DSNQ_ERR_UNSUPPORTED;
     prm.total_tiles = static_cast<int>(total);
+    prm.total_super = static_cast<int>(total_super);
     const uint64_t tmo = g_timeout_ns.load();
     prm.timeout_ns = tmo ? tmo : kDefaultTimeoutNs;
     prm.inject = g_inject.load();
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (paired) return launch_pair(prm, ma, mw[0], mw[1], mo[0], mo[1], s);
     switch (bn) {
         // Decode: the MMA per K block is tiny, so the MMA <-> promotion round
         // trip sets the pace; a TMEM ring as deep as TMEM allows (512 / BN

@@ -48,8 +48,11 @@ def check_gemm(got_bf16: torch.Tensor, a_codes, a_scale, w_codes, w_scale, rows=
     return err
 
 
+# From 256 rows on the GEMM runs in 2 x 2 clusters: odd tile counts along
+# either side (300, 520 rows; 128, 272, 656 features) leave padding tiles.
 SHAPES = [(1, 128, 128), (3, 256, 256), (16, 512, 1536), (17, 272, 512), (40, 4096, 1536),
-          (64, 384, 1536), (65, 256, 384), (128, 512, 1536), (200, 1024, 1536), (300, 272, 768)]
+          (64, 384, 1536), (65, 256, 384), (128, 512, 1536), (200, 1024, 1536), (300, 272, 768),
+          (256, 128, 1536), (520, 656, 256), (1000, 400, 1280)]
 
 
 @pytest.mark.parametrize("M,N,K", SHAPES)
@@ -177,7 +180,7 @@ def test_gemm_zero_rows():
     assert out.shape == (0, 256)
 
 
-@pytest.mark.parametrize("M", [4, 200])
+@pytest.mark.parametrize("M", [4, 200, 512])
 def test_bounded_wait_times_out_and_context_survives(M):
     """The producer skips its first load on purpose; the consumer's bounded
     wait runs out, the kernel records a timeout and returns, and the next
