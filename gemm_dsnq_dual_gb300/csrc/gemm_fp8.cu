@@ -854,10 +854,17 @@ constexpr size_t smem_bytes(int KB) {
 // release a TMEM buffer on the even CTA's barrier.  Each promotion thread
 // carries 64 fp32 accumulators, so the role warps give up registers
 // (setmaxnreg) to the promotion warps.
+//
+// A K block is issued as two column halves (MMA N=128 each) into their own
+// TMEM buffers, so the promotion of half 0 starts while the tensor core
+// works on half 1; TMEM holds two K blocks of both halves.  For an N=128
+// MMA each CTA supplies 64 weight rows, so CTA r stores weight rows
+// 128h + 64r .. +63 of the tile as chunk h of its stage.
 namespace pair {
 constexpr int kBN = 256;                        // output columns of a tile (both CTAs)
+constexpr int kHalfN = 128;                     // MMA N of one column half
 constexpr int kStages = 5;
-constexpr int kNBuf = 2;                        // TMEM partial buffers of 256 columns
+constexpr int kNBuf = 2;                        // K blocks in TMEM (x 2 halves of 128 columns)
 constexpr int kEpiWarps = 16;
 constexpr int kThreads = (4 + kEpiWarps) * 32;
 constexpr int kHalfBytes = kPRows * kBK;        // 16 KB: 128 rows x 128 K bytes
@@ -867,7 +874,7 @@ constexpr int kLdCols = 16;                     // columns per TMEM load
 constexpr int kStageOutBytes = 32 * 32 * 2;     // one 32 x 32 bf16 block per promotion warp
 constexpr int kTmemCols = 512;
 constexpr uint32_t kRegsLaunch = 96;            // 65536 / 640, in steps of 8
-constexpr uint32_t kRegsRole = 56;
+constexpr uint32_t kRegsRole = 64;
 constexpr uint32_t kRegsEpi = 104;
 static_assert(4 * 32 * kRegsRole + kEpiWarps * 32 * kRegsEpi <= kThreads * kRegsLaunch,
               "the register split must fit in what the block is launched with");
@@ -942,14 +949,14 @@ __device__ __forceinline__ void tc_commit_pair_local(uint32_t bar) {
         "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
         : "memory");
 }
-// Instruction descriptor: D fp32, A and B E4M3, K-major, M = 256, N = 256.
+// Instruction descriptor: D fp32, A and B E4M3, K-major, M = 256, N = 128.
 __host__ __device__ constexpr uint32_t idesc_e4m3_pair() {
-    return (1u << 4) | (static_cast<uint32_t>(kBN >> 3) << 17) | (static_cast<uint32_t>(256 >> 4) << 24);
+    return (1u << 4) | (static_cast<uint32_t>(kHalfN >> 3) << 17) | (static_cast<uint32_t>(256 >> 4) << 24);
 }
 
 constexpr size_t smem_bytes(int KB) {
     const int KBP = (KB + 3) & ~3;
-    return 1024 + kStages * kStageBytes + kEpiWarps * kStageOutBytes + (2 * kStages + 2 * kNBuf + 5) * 8 + 32 +
+    return 1024 + kStages * kStageBytes + kEpiWarps * kStageOutBytes + (2 * kStages + 4 * kNBuf + 5) * 8 + 32 +
            static_cast<size_t>(2 * KBP * kPRows + 2 * 2 * KBP) * 4;
 }
 }  // namespace pair
@@ -966,9 +973,9 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
     uint64_t* bars = reinterpret_cast<uint64_t*>(out_stage + kEpiWarps * kStageOutBytes);
     uint64_t* full = bars;                    // [S]  even CTA: both CTAs' loads of a stage
     uint64_t* empty = bars + kStages;         // [S]  MMA -> TMA (multicast to both)
-    uint64_t* tfull = bars + 2 * kStages;     // [NB] MMA -> promotion (multicast to both)
-    uint64_t* tempty = tfull + kNBuf;         // [NB] even CTA: both CTAs' promotion -> gate
-    uint64_t* sfull = tempty + kNBuf;         // [2]
+    uint64_t* tfull = bars + 2 * kStages;     // [2 halves][NB] MMA -> promotion (multicast to both)
+    uint64_t* tempty = tfull + 2 * kNBuf;     // [2 halves][NB] even CTA: both CTAs' promotion -> gate
+    uint64_t* sfull = tempty + 2 * kNBuf;     // [2]
     uint64_t* sempty = sfull + 2;             // [2]
     uint64_t* drain = sempty + 2;             // [1]
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
@@ -999,9 +1006,9 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
             mbar_init(smem_u32(&full[s]), 1);
             mbar_init(smem_u32(&empty[s]), 1);
         }
-        for (int b = 0; b < kNBuf; ++b) {
+        for (int b = 0; b < 2 * kNBuf; ++b) {
             mbar_init(smem_u32(&tfull[b]), 1);
-            mbar_init(smem_u32(&tempty[b]), 2 * kEpiWarps);
+            mbar_init(smem_u32(&tempty[b]), kEpiWarps);   // the 8 warps of a half, in both CTAs
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(&sfull[i]), 32);
@@ -1035,11 +1042,11 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
     if (warp < 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsRole));
     if (warp == 0) {
-        // ------------------------------------------------ TMA producer (2*S lanes, both CTAs)
-        if (lane < 2 * kStages) {
+        // ------------------------------------------------ TMA producer (3*S lanes, both CTAs)
+        if (lane < 3 * kStages) {
             const uint32_t ng = static_cast<uint32_t>(items) * KB;
-            const int s = lane >> 1;
-            const bool loads_w = lane & 1;
+            const int s = lane / 3;
+            const int part = lane % 3;           // 0: activation rows, 1/2: weight chunk 0/1
             const uint32_t fb = peer_addr(smem_u32(&full[s]), 0);   // the even CTA's stage barrier
             uint8_t* st = tiles + s * kStageBytes;
             uint32_t last = 0;
@@ -1053,12 +1060,13 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
                 const int tl = static_cast<int>(g / KB), kb = static_cast<int>(g % KB);
                 int pi, m0, n0;
                 coords(first + tl * stride, pi, m0, n0);
-                if (!loads_w) {
+                if (part == 0) {
                     if (even) mbar_arrive_expect_tx(smem_u32(&full[s]), 2 * kStageBytes);
                     tma_load_2d_pair(smem_u32(st), &map_a, fb, kb * kBK, m0);
                 } else {
-                    tma_load_2d_pair(smem_u32(st + kHalfBytes), pi ? &map_w1 : &map_w0, fb, kb * kBK,
-                                     n0 + static_cast<int>(rank) * kPRows);
+                    const int h = part - 1;
+                    tma_load_2d_pair(smem_u32(st + kHalfBytes + h * (kHalfBytes / 2)), pi ? &map_w1 : &map_w0, fb,
+                                     kb * kBK, n0 + h * kHalfN + static_cast<int>(rank) * (kHalfN / 2));
                 }
                 last = g + 1;
             }
@@ -1078,25 +1086,32 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
             const uint64_t dw0 = smem_desc_k_sw128(smem_u32(tiles + kHalfBytes));
             uint32_t g = 0, ready = 0;
             bool ok = true, any = false;
+            // The gate counts column halves: half h of K block g may be issued
+            // once the count exceeds 2g + h.
             for (int it = 0; it < items && ok; ++it) {
-                for (int kb = 0; kb < KB; ++kb, ++g) {
+                for (int kb = 0; kb < KB && ok; ++kb, ++g) {
                     const int s = g % kStages;
-                    const int b = g % kNBuf;
-                    if (g >= ready && !wait_gate(smem_u32(gate), g, ready, abort_flag, tmo)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
+                    const int q = g % kNBuf;
                     const uint64_t so = static_cast<uint64_t>((s * kStageBytes) >> 4);
-                    const uint32_t d = tmem_base + static_cast<uint32_t>(b * kBN);
 #pragma unroll
-                    for (int k = 0; k < kBK / kUmmaK; ++k) {
-                        const uint64_t ko = so + static_cast<uint64_t>((k * kUmmaK) >> 4);
-                        tc_mma_f8_pair(d, da0 + ko, dw0 + ko, idesc, k > 0 ? 1u : 0u);
+                    for (int h = 0; h < 2; ++h) {
+                        const uint32_t need = 2 * g + h;
+                        if (need >= ready && !wait_gate(smem_u32(gate), need, ready, abort_flag, tmo)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t d = tmem_base + static_cast<uint32_t>((2 * h + q) * kHalfN);
+                        const uint64_t wo = so + static_cast<uint64_t>((h * (kHalfBytes / 2)) >> 4);
+#pragma unroll
+                        for (int k = 0; k < kBK / kUmmaK; ++k) {
+                            const uint64_t ko = static_cast<uint64_t>((k * kUmmaK) >> 4);
+                            tc_mma_f8_pair(d, da0 + so + ko, dw0 + wo + ko, idesc, k > 0 ? 1u : 0u);
+                        }
+                        if (h == 1) tc_commit_pair_both(smem_u32(&empty[s]));
+                        tc_commit_pair_both(smem_u32(&tfull[h * kNBuf + q]));
+                        any = true;
                     }
-                    tc_commit_pair_both(smem_u32(&empty[s]));
-                    tc_commit_pair_both(smem_u32(&tfull[b]));
-                    any = true;
                 }
             }
             if (*abort_flag && any) {
@@ -1112,12 +1127,18 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
             bool ok = true;
             for (int it = 0; it < items && ok; ++it) {
                 for (int kb = 0; kb < KB; ++kb, ++g) {
+                    const uint32_t q = g % kNBuf, par = ((g / kNBuf) & 1) ^ 1;
                     if (!wait_bounded<true>(smem_u32(&full[g % kStages]), (g / kStages) & 1, abort_flag, tmo) ||
-                        !wait_bounded<true>(smem_u32(&tempty[g % kNBuf]), ((g / kNBuf) & 1) ^ 1, abort_flag, tmo)) {
+                        !wait_bounded<true>(smem_u32(&tempty[q]), par, abort_flag, tmo)) {
                         ok = false;
                         break;
                     }
-                    st_release_shared(smem_u32(gate), g + 1);
+                    st_release_shared(smem_u32(gate), 2 * g + 1);
+                    if (!wait_bounded<true>(smem_u32(&tempty[kNBuf + q]), par, abort_flag, tmo)) {
+                        ok = false;
+                        break;
+                    }
+                    st_release_shared(smem_u32(gate), 2 * g + 2);
                 }
             }
         }
@@ -1174,9 +1195,11 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
         const int slice = ew >> 2;               // columns 64*slice .. +63 of the tile
         const int row = quarter * 32 + lane;
         const int col0 = slice * kCols;
-        static_assert(kNBuf == 2, "two buffer-free barriers in the even CTA");
-        const uint32_t tempty_even0 = peer_addr(smem_u32(&tempty[0]), 0);
-        const uint32_t tempty_even1 = peer_addr(smem_u32(&tempty[1]), 0);
+        static_assert(kNBuf == 2, "two buffer-free barriers per half in the even CTA");
+        const int half = slice >> 1;             // column half of the tile (its own MMA and buffers)
+        const int hcol = (slice & 1) * kCols;    // columns within the half
+        const uint32_t tempty_even0 = peer_addr(smem_u32(&tempty[half * kNBuf + 0]), 0);
+        const uint32_t tempty_even1 = peer_addr(smem_u32(&tempty[half * kNBuf + 1]), 0);
         uint32_t g = 0;
         bool ok = true;
         for (int i = 0; i < items && ok; ++i) {
@@ -1203,7 +1226,7 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
                     w_nxt = sw_t[kb + 1];
                 }
                 const int b = g % kNBuf;
-                const bool got = wait_bounded<true>(smem_u32(&tfull[b]), (g / kNBuf) & 1, abort_flag, tmo);
+                const bool got = wait_bounded<true>(smem_u32(&tfull[half * kNBuf + b]), (g / kNBuf) & 1, abort_flag, tmo);
                 if (!__all_sync(0xffffffffu, got)) {
                     ok = false;
                     break;
@@ -1211,7 +1234,7 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
                 tc_fence_after();
                 const float2 s2 = make_float2(sk, sk);
                 const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
-                                       static_cast<uint32_t>(b * kBN + col0);
+                                       static_cast<uint32_t>((2 * half + b) * kHalfN + hcol);
 #pragma unroll
                 for (int h = 0; h < kCols / kLdCols; ++h) {
                     uint64_t r[kLdCols / 2];
@@ -1224,7 +1247,7 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
                 __syncwarp();
                 if (lane == 0) {
                     if (even)
-                        mbar_arrive(smem_u32(&tempty[b]));
+                        mbar_arrive(smem_u32(&tempty[half * kNBuf + b]));
                     else
                         mbar_arrive_remote(b ? tempty_even1 : tempty_even0);
                 }
@@ -1445,7 +1468,9 @@ dsnq_status run_gemm(int64_t M, int64_t K, const void* a, int64_t lda, const flo
     const bool paired = !swap && M >= 256;
     const int bn = swap ? (M <= 16 ? 16 : M <= 32 ? 32 : 64) : 128;
     const int a_box = swap ? bn : gemm::kPRows;
-    const int w_box = swap ? gemm::kPRows : bn;
+    // The CTA-pair kernel loads weight rows in chunks of 64 (each CTA's share
+    // of an N=128 MMA).
+    const int w_box = swap ? gemm::kPRows : (paired ? gemm::pair::kHalfN / 2 : bn);
 
     gemm::Params prm{};
     prm.M = static_cast<int>(M);
