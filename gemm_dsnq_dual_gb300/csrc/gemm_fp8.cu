@@ -304,6 +304,25 @@ __device__ __forceinline__ void tmem_ld_pairs<16>(uint32_t taddr, uint64_t (&r)[
         : "memory");
 }
 
+// Split form for software pipelining: the load is issued by one statement and
+// completed by another, which takes the destination registers as operands so
+// that no use of them can be scheduled before the wait.
+__device__ __forceinline__ void tmem_ld16_issue(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_ld16_wait(uint32_t (&r)[16]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                   "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
+                 :
+                 : "memory");
+}
+
 template <>
 __device__ __forceinline__ void tmem_ld_pairs<32>(uint32_t taddr, uint64_t (&r)[16]) {
     asm volatile(
@@ -863,7 +882,7 @@ constexpr size_t smem_bytes(int KB) {
 namespace pair {
 constexpr int kBN = 256;                        // output columns of a tile (both CTAs)
 constexpr int kHalfN = 128;                     // MMA N of one column half
-constexpr int kStages = 5;
+constexpr int kStages = 4;
 constexpr int kNBuf = 2;                        // K blocks in TMEM (x 2 halves of 128 columns)
 constexpr int kEpiWarps = 16;
 constexpr int kThreads = (4 + kEpiWarps) * 32;
@@ -871,7 +890,7 @@ constexpr int kHalfBytes = kPRows * kBK;        // 16 KB: 128 rows x 128 K bytes
 constexpr int kStageBytes = 2 * kHalfBytes;     // this CTA's activation rows + weight rows
 constexpr int kCols = 64;                       // accumulator columns per promotion thread
 constexpr int kLdCols = 16;                     // columns per TMEM load
-constexpr int kStageOutBytes = 32 * 32 * 2;     // one 32 x 32 bf16 block per promotion warp
+constexpr int kStageOutBytes = 32 * kCols * 2;  // a promotion warp's 32 x 64 bf16 block
 constexpr int kTmemCols = 512;
 constexpr uint32_t kRegsLaunch = 96;            // 65536 / 640, in steps of 8
 constexpr uint32_t kRegsRole = 64;
@@ -1235,14 +1254,28 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
                 const float2 s2 = make_float2(sk, sk);
                 const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                        static_cast<uint32_t>((2 * half + b) * kHalfN + hcol);
+                // Four 16-column loads, each issued while the previous chunk is
+                // added in; the buffer is released as soon as the last load has
+                // completed, before its chunk is added.
+                static_assert(kCols == 4 * kLdCols && kLdCols == 16, "four 16-column chunks");
+                uint32_t ra[16], rb[16];
+                auto add = [&](int h, const uint32_t (&r)[16]) {
 #pragma unroll
-                for (int h = 0; h < kCols / kLdCols; ++h) {
-                    uint64_t r[kLdCols / 2];
-                    tmem_ld_pairs<kLdCols>(tbase + h * kLdCols, r);
-#pragma unroll
-                    for (int j = 0; j < kLdCols / 2; ++j)
-                        acc[h * (kLdCols / 2) + j] = __ffma2_rn(as_float2(r[j]), s2, acc[h * (kLdCols / 2) + j]);
-                }
+                    for (int j = 0; j < 8; ++j)
+                        acc[h * 8 + j] = __ffma2_rn(make_float2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1])),
+                                                    s2, acc[h * 8 + j]);
+                };
+                tmem_ld16_issue(tbase, ra);
+                tmem_ld16_wait(ra);
+                tmem_ld16_issue(tbase + 16, rb);
+                add(0, ra);
+                tmem_ld16_wait(rb);
+                tmem_ld16_issue(tbase + 32, ra);
+                add(1, rb);
+                tmem_ld16_wait(ra);
+                tmem_ld16_issue(tbase + 48, rb);
+                add(2, ra);
+                tmem_ld16_wait(rb);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) {
@@ -1251,37 +1284,32 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
                     else
                         mbar_arrive_remote(b ? tempty_even1 : tempty_even0);
                 }
+                add(3, rb);
                 ++g;
             }
             if (!ok) break;
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&sempty[slot]));
 
-            // Epilogue: this warp's 32 rows x 64 columns, as two 32 x 32 bf16
-            // blocks through one 64-byte-swizzled staging buffer.
-            uint8_t* stg = out_stage + ew * kStageOutBytes;
-            const int r0 = m0 + quarter * 32;
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                const int c0 = n0 + col0 + half * 32;
-                if (lane == 0) bulk_wait_read_all();
+            // Epilogue: this warp's 32 rows x 64 columns as bf16 into its
+            // staging buffer (128-byte rows, 128-byte swizzle: 16-byte chunk c
+            // of row r at chunk c ^ (r & 7)), then one TMA store.
+            if (m0 + quarter * 32 < p.M && n0 + col0 < pr.N) {
+                uint8_t* stg = out_stage + ew * kStageOutBytes;
+                if (lane == 0) bulk_wait_read_all();   // the previous tile's store has read the buffer
                 __syncwarp();
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
+                for (int c = 0; c < kCols / 8; ++c) {
                     uint4 v;
                     __nv_bfloat162* hv = reinterpret_cast<__nv_bfloat162*>(&v);
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const float2 a = acc[half * 16 + 4 * c + q];
-                        hv[q] = __floats2bfloat162_rn(a.x, a.y);
-                    }
-                    const int sc = c ^ ((lane >> 1) & 3);
-                    *reinterpret_cast<uint4*>(stg + lane * 64 + sc * 16) = v;
+                    for (int q = 0; q < 4; ++q) hv[q] = __floats2bfloat162_rn(acc[4 * c + q].x, acc[4 * c + q].y);
+                    *reinterpret_cast<uint4*>(stg + lane * (kCols * 2) + ((c ^ (lane & 7)) * 16)) = v;
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0 && r0 < p.M && c0 < pr.N) {
-                    tma_store_2d(pi ? &map_o1 : &map_o0, smem_u32(stg), c0, r0);
+                if (lane == 0) {
+                    tma_store_2d(pi ? &map_o1 : &map_o0, smem_u32(stg), n0 + col0, m0 + quarter * 32);
                     bulk_commit();
                 }
             }
@@ -1340,16 +1368,18 @@ bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t K, int64_t
 // 2-D map over a bf16 output [rows, cols] with row stride ld elements; box =
 // 32 columns (64 bytes) x 32 rows, 64-byte swizzle (the staging layout of the
 // epilogue); stores past the extent are clipped.
-bool make_out_map(CUtensorMap* m, void* base, int64_t rows, int64_t cols, int64_t ld) {
+// box_cols = 32 (64-byte rows, 64-byte swizzle) or 64 (128-byte rows,
+// 128-byte swizzle), 32 rows.
+bool make_out_map(CUtensorMap* m, void* base, int64_t rows, int64_t cols, int64_t ld, int box_cols) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld * 2)};
-    cuuint32_t box[2] = {32, 32};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), 32};
     cuuint32_t estr[2] = {1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-              CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
-           CUDA_SUCCESS;
+              box_cols == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 std::atomic<uint32_t> g_inject{0};
@@ -1501,7 +1531,7 @@ dsnq_status run_gemm(int64_t M, int64_t K, const void* a, int64_t lda, const flo
         pr.out = static_cast<__nv_bfloat16*>(c.out);
         pr.ldo = c.ldo;
         if (!make_map(&mw[np], c.w, c.N, K, c.ldw, w_box)) return DSNQ_ERR_CUDA;
-        if (!swap && !make_out_map(&mo[np], c.out, M, c.N, c.ldo)) return DSNQ_ERR_CUDA;
+        if (!swap && !make_out_map(&mo[np], c.out, M, c.N, c.ldo, paired ? 64 : 32)) return DSNQ_ERR_CUDA;
         const int64_t tiles = static_cast<int64_t>(prm.tiles_m) * pr.tiles_n;
         const int64_t supers = static_cast<int64_t>(prm.tiles_m2) * ((c.N + 255) / 256);
         if (np == 0) {
