@@ -393,6 +393,173 @@ warp_row_kernel(const RowArgs a) {
     }
 }
 
+struct GroupQuant {
+    float scale;            // amax / 448, IEEE fp32
+    float2 ylo, yhi;        // fp32(1/scale) * (1 -+ 2^-20), rounded: bracket the quotient
+    bool exact;             // reciprocal not finite: divide
+};
+
+__device__ __forceinline__ GroupQuant make_group_quant(float amax) {
+    GroupQuant gq;
+    gq.scale = amax / kE4M3Max;                       // IEEE fp32 divide
+    gq.exact = gq.scale > 0.f && gq.scale < 1.0e-36f;
+    const float y = (gq.scale > 0.f && !gq.exact) ? __fdividef(1.0f, gq.scale) : 0.f;
+    // y is within 2^-22 of 1/scale; each product below adds at most 2^-24,
+    // so x*ylo <= x/scale <= x*yhi (in magnitude order) with room to spare.
+    const float lo = y * (1.0f - 0x1p-20f), hi = y * (1.0f + 0x1p-20f);
+    gq.ylo = make_float2(lo, lo);
+    gq.yhi = make_float2(hi, hi);
+    return gq;
+}
+
+// Codes of eight values by the bracket; *ok is false when a code is not
+// determined (or the group needs the division).
+__device__ __forceinline__ uint2 quant8_bracket(const float2 (&f)[4], const GroupQuant& gq, bool& ok) {
+    uint32_t lo[2], hi[2];
+#pragma unroll
+    for (int w = 0; w < 2; ++w) {
+        lo[w] = e4m3x2(mul2(f[2 * w], gq.ylo)) | (e4m3x2(mul2(f[2 * w + 1], gq.ylo)) << 16);
+        hi[w] = e4m3x2(mul2(f[2 * w], gq.yhi)) | (e4m3x2(mul2(f[2 * w + 1], gq.yhi)) << 16);
+    }
+    ok = lo[0] == hi[0] && lo[1] == hi[1] && !gq.exact;
+    return make_uint2(lo[0], lo[1]);
+}
+
+// ---------------------------------------------------------------------------
+// Fused warp-per-row kernel for rows whose q and kv parts are whole warp
+// slots (Kq and Kkv multiples of 256: QS slots of q, KS of kv; DSv4: 6 + 2).
+//   * each slot's role is known at compile time (no per-chunk predicates);
+//   * the next row of the warp is loaded into registers while the current
+//     one is processed;
+//   * the row is processed in phases over all slots (sums of squares, norm,
+//     group amax, scales, codes) so that the independent chains overlap;
+//   * the quantize step uses bracket reciprocals scaled once per group and
+//     takes the exactness decision for the whole row with one warp vote.
+// ---------------------------------------------------------------------------
+constexpr int kFusedCtasPerSM = 3;  // register budget: 168 per thread
+
+template <int QS, int KS>
+__global__ void __launch_bounds__(kRowWarps * 32, kFusedCtasPerSM)
+warp_row_fused_kernel(const RowArgs a) {
+    constexpr int CPT = QS + KS;
+    extern __shared__ float gamma_s[];          // [(QS + KS) * 256] fp32: gamma_q then gamma_kv
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    constexpr int kq = QS * 256, width = CPT * 256;
+
+    auto load_row = [&](int64_t m, uint4 (&raw)[CPT]) {
+#pragma unroll
+        for (int j = 0; j < CPT; ++j) {
+            const __nv_bfloat16* src = j < QS ? a.q + m * a.ldq + (j * 32 + lane) * kChunk
+                                              : a.kv + m * a.ldkv + ((j - QS) * 32 + lane) * kChunk;
+            raw[j] = __ldg(reinterpret_cast<const uint4*>(src));
+        }
+    };
+
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kRowWarps;
+    int64_t m = static_cast<int64_t>(blockIdx.x) * kRowWarps + warp;
+    uint4 cur[CPT];
+    if (m < a.M) load_row(m, cur);               // in flight while gamma is staged
+
+    for (int i = threadIdx.x * kChunk; i < width; i += kRowWarps * 32 * kChunk) {
+        const __nv_bfloat16* gsrc = i < kq ? a.gamma_q + i : a.gamma_kv + (i - kq);
+        float2 g[4];
+        unpack8(__ldg(reinterpret_cast<const uint4*>(gsrc)), g);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) reinterpret_cast<float2*>(gamma_s + i)[k] = g[k];
+    }
+    __syncthreads();
+
+    for (; m < a.M; m += stride) {
+        uint4 nxt[CPT];
+        const int64_t mn = m + stride;
+        if (mn < a.M) load_row(mn, nxt);         // prefetch this warp's next row
+        float2 x[CPT][4];
+#pragma unroll
+        for (int j = 0; j < CPT; ++j) unpack8(cur[j], x[j]);
+        float2 sq[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+        float2 skv[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+        for (int j = 0; j < CPT; ++j) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                if (j < QS) sq[i & 1] = fma2(x[j][i], x[j][i], sq[i & 1]);
+                else skv[i & 1] = fma2(x[j][i], x[j][i], skv[i & 1]);
+            }
+        }
+        const float ssq_q = warp_sum((sq[0].x + sq[1].x) + (sq[0].y + sq[1].y));
+        const float ssq_kv = warp_sum((skv[0].x + skv[1].x) + (skv[0].y + skv[1].y));
+        // Correctly rounded sqrt and divide (not the approximate rsqrt).
+        const float rq = 1.0f / sqrtf(ssq_q / a.kq_f + a.eps);
+        const float rkv = 1.0f / sqrtf(ssq_kv / a.kkv_f + a.eps);
+
+        // Normalize; kv goes straight out.
+#pragma unroll
+        for (int j = 0; j < CPT; ++j) {
+            const int col = (j < QS ? j : j - QS) * 256 + lane * kChunk;
+            const float r = j < QS ? rq : rkv;
+            const float2 r2 = make_float2(r, r);
+            const float4* gp = reinterpret_cast<const float4*>(gamma_s + (j < QS ? 0 : kq) + col);
+            const float4 g0 = gp[0], g1 = gp[1];
+            x[j][0] = mul2(mul2(x[j][0], r2), make_float2(g0.x, g0.y));
+            x[j][1] = mul2(mul2(x[j][1], r2), make_float2(g0.z, g0.w));
+            x[j][2] = mul2(mul2(x[j][2], r2), make_float2(g1.x, g1.y));
+            x[j][3] = mul2(mul2(x[j][3], r2), make_float2(g1.z, g1.w));
+            if (j >= QS) *reinterpret_cast<uint4*>(a.kv_out + m * a.ldkv_out + col) = pack8_bf16(x[j]);
+        }
+
+        // Group amax (one 128-column group per half-warp and q slot).
+        float am[QS];
+#pragma unroll
+        for (int j = 0; j < QS; ++j)
+            am[j] = fmaxf(fmaxf(fmaxf(fabsf(x[j][0].x), fabsf(x[j][0].y)), fmaxf(fabsf(x[j][1].x), fabsf(x[j][1].y))),
+                          fmaxf(fmaxf(fabsf(x[j][2].x), fabsf(x[j][2].y)), fmaxf(fabsf(x[j][3].x), fabsf(x[j][3].y))));
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) {
+#pragma unroll
+            for (int j = 0; j < QS; ++j) am[j] = fmaxf(am[j], __shfl_xor_sync(0xffffffffu, am[j], o));
+        }
+
+        // Scales and codes.
+        GroupQuant gq[QS];
+        uint2 codes[QS];
+        bool ok_all = true;
+#pragma unroll
+        for (int j = 0; j < QS; ++j) {
+            gq[j] = make_group_quant(am[j]);
+            bool ok;
+            codes[j] = quant8_bracket(x[j], gq[j], ok);
+            ok_all = ok_all && ok;
+        }
+        if (!__all_sync(0xffffffffu, ok_all)) {
+            // Rare: a code within 2^-20 of a rounding boundary, or a scale
+            // that is zero or too small for a reciprocal: the division itself
+            // (x * 0 keeps the sign of zero codes of a zero group).
+#pragma unroll
+            for (int j = 0; j < QS; ++j) {
+                bool ok;
+                quant8_bracket(x[j], gq[j], ok);
+                if (ok) continue;
+                const float sc = gq[j].scale;
+                float2 qv[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    qv[i] = sc > 0.f ? make_float2(__fdiv_rn(x[j][i].x, sc), __fdiv_rn(x[j][i].y, sc))
+                                     : make_float2(x[j][i].x * 0.f, x[j][i].y * 0.f);
+                codes[j] = make_uint2(e4m3x2(qv[0]) | (e4m3x2(qv[1]) << 16), e4m3x2(qv[2]) | (e4m3x2(qv[3]) << 16));
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < QS; ++j) {
+            const int col = j * 256 + lane * kChunk;
+            *reinterpret_cast<uint2*>(a.q_fp8 + m * a.ldq_out + col) = codes[j];
+            if ((lane & 15) == 0) a.scale[m * a.scale_row_stride + (col / 128) * a.scale_group_stride] = gq[j].scale;
+        }
+    #pragma unroll
+        for (int j = 0; j < CPT; ++j) cur[j] = nxt[j];
+    }
+}
+
 template <int MODE>
 static dsnq_status launch_rows(RowArgs a, int64_t M, cudaStream_t s) {
     const int chunks = a.cq + a.ckv;
@@ -402,6 +569,14 @@ static dsnq_status launch_rows(RowArgs a, int64_t M, cudaStream_t s) {
     // Many rows: one warp per row (no block barrier per row).  Few rows: a
     // warp-group per row, which shortens each thread's dependency chain.
     const int64_t warp_row_min = sms > 0 ? static_cast<int64_t>(sms) * 8 : 2048;
+    if (MODE == kFused && a.cq == 6 * 32 && a.ckv == 2 * 32 && M >= warp_row_min) {
+        // DSv4 rows (Kq = 1536, Kkv = 512): the specialized warp-per-row kernel.
+        const int64_t rows_cap = sms > 0 ? static_cast<int64_t>(sms) * kFusedCtasPerSM : (M + kRowWarps - 1) / kRowWarps;
+        const int64_t need = (M + kRowWarps - 1) / kRowWarps;
+        dim3 grid(static_cast<unsigned>(need < rows_cap ? need : rows_cap)), block(kRowWarps * 32);
+        warp_row_fused_kernel<6, 2><<<grid, block, static_cast<size_t>(chunks) * kChunk * sizeof(float), s>>>(a);
+        return launch_status();
+    }
     if (chunks <= 8 * 32 && M >= warp_row_min) {
         // Warp per row.  Enough CTAs to fill every SM at the register-limited occupancy.
         const int cpt = (chunks + 31) / 32;
