@@ -348,10 +348,26 @@ def side_measurements(torch, dsnq, inputs, dev, flush, hbm_gbs, args):
                          "fused_frac_hbm": round(gbs / hbm_gbs, 4),
                          "unfused_3_kernels_us": round(u_us, 3),
                          "speedup_vs_unfused": round(u_us / f_us, 3)}
+        # Back-to-back calls: a CUDA graph over distinct input/output sets
+        # whose total exceeds L2, so every call reads from and writes to HBM.
+        nsets = max(2, -(-160 * 2 ** 20 // (M * NQ_BYTES_PER_ROW)))
+        if nsets * M * NQ_BYTES_PER_ROW <= 2 * 2 ** 30:
+            sets = [(q.clone(), kv.clone(), torch.empty_like(qf), dsnq.empty_scales(M, KQ // 128, "col", dev),
+                     torch.empty_like(ko2)) for _ in range(nsets)]
+            calls = [(lambda t=t: dsnq.fused_dual_rmsnorm_group_quant(
+                t[0], t[1], gq2, gkv2, lat.eps, scale_layout="col", q_out=t[2], q_scale=t[3], kv_out=t[4]))
+                for t in sets]
+            g_us = timed_graph_calls(torch, stream, calls, flush, reps=max(args.side_reps, 5))
+            g_gbs = (M * NQ_BYTES_PER_ROW + NQ_BYTES_PER_CALL) / (g_us * 1e-6) / 1e9
+            sweep[str(M)].update({"fused_graph_us": round(g_us, 3), "fused_graph_gbs": round(g_gbs, 1),
+                                  "fused_graph_frac_hbm": round(g_gbs / hbm_gbs, 4), "graph_sets": nsets})
+            del sets, calls
         del q, kv, qf, sc, ko2, qb, qf2, sc2
     out["norm_quant_sweep"] = sweep
-    out["norm_quant_sweep_note"] = ("single launches timed with CUDA events, L2 flushed before each; "
-                                    "M=8192 uses the prefill Student-t inputs, column-major scales")
+    out["norm_quant_sweep_note"] = ("fused_us / unfused: single launches timed with CUDA events, L2 flushed before "
+                                    "each (includes launch latency); fused_graph_us: per call in a CUDA graph of "
+                                    "back-to-back calls over graph_sets distinct input/output sets (> 160 MiB in "
+                                    "total, more than L2); M=8192 uses the prefill Student-t inputs, column-major scales")
     return out
 
 
@@ -363,6 +379,7 @@ def gemm_sweep(torch, dsnq, inputs, dev, flush, hbm_gbs, args):
     wi, swi = dsnq.quantize_weight_block128(inputs.weight(N_IDX, KQ, seed=0, salt=2).to(dev))
     wbytes = (N_ATTN + N_IDX) * KQ
     res = {}
+    copies = []
     for M in args.gemm_sweep:
         a, sa = inputs.random_codes_and_scales(M, KQ, seed=M)
         a, sa = a.to(dev), sa.to(dev)
@@ -374,6 +391,20 @@ def gemm_sweep(torch, dsnq, inputs, dev, flush, hbm_gbs, args):
         res[str(M)] = {"us": round(us, 3), "tflops": round(gemm_flops(M) / (us * 1e-6) / 1e12, 1),
                        "gbs": round(byt / (us * 1e-6) / 1e9, 1),
                        "frac_hbm": round(byt / (us * 1e-6) / 1e9 / hbm_gbs, 4)}
+        if M <= 128:
+            # Back-to-back calls as in a decode loop: a CUDA graph of 8 calls over
+            # 4 copies of the weights (176 MB, more than L2), so each call streams
+            # its weights from HBM without the per-launch host and event overhead.
+            if not copies:
+                copies.extend([(wa, swa, wi, swi)] + [(wa.clone(), swa.clone(), wi.clone(), swi.clone())
+                                                      for _ in range(3)])
+            calls = [(lambda c=copies[i % 4]: dsnq.block_scaled_fp8_gemm_dual(
+                a, sa, c[0], c[1], c[2], c[3], out1=oa, out2=oi)) for i in range(8)]
+            gus = timed_graph_calls(torch, stream, calls, flush, reps=max(args.side_reps, 5))
+            res[str(M)].update({"graph_us": round(gus, 3), "graph_gbs": round(byt / (gus * 1e-6) / 1e9, 1),
+                                "graph_frac_hbm": round(byt / (gus * 1e-6) / 1e9 / hbm_gbs, 4)})
+    res["note"] = ("us: one launch timed with CUDA events after an L2 flush (includes launch latency); "
+                   "graph_us: per call in a CUDA graph of 8 back-to-back calls over 4 weight copies (cold in L2)")
     return res
 
 

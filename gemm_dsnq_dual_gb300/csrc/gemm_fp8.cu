@@ -48,6 +48,8 @@
 
 #include <atomic>
 #include <mutex>
+#include <tuple>
+#include <vector>
 
 #include "dsnq_internal.h"
 
@@ -1366,10 +1368,9 @@ bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t K, int64_t
 }
 
 // 2-D map over a bf16 output [rows, cols] with row stride ld elements; box =
-// 32 columns (64 bytes) x 32 rows, 64-byte swizzle (the staging layout of the
-// epilogue); stores past the extent are clipped.
-// box_cols = 32 (64-byte rows, 64-byte swizzle) or 64 (128-byte rows,
-// 128-byte swizzle), 32 rows.
+// box_cols x 32 rows, box_cols = 32 (64-byte rows, 64-byte swizzle) or 64
+// (128-byte rows, 128-byte swizzle), the staging layouts of the epilogues;
+// stores past the extent are clipped.
 bool make_out_map(CUtensorMap* m, void* base, int64_t rows, int64_t cols, int64_t ld, int box_cols) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
@@ -1380,6 +1381,90 @@ bool make_out_map(CUtensorMap* m, void* base, int64_t rows, int64_t cols, int64_
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
               box_cols == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Encoding a tensor map is host work of a few microseconds, comparable to a
+// decode-size GEMM, so maps are kept in a small cache.  A map only describes
+// address arithmetic (base, extents, strides, box), so a cached map stays
+// valid for its key whatever the memory holds.
+struct MapKey {
+    const void* base;
+    int64_t rows, cols, ld;
+    int box, kind;          // kind 0: operand map, 1: output map
+    bool operator==(const MapKey& o) const {
+        return base == o.base && rows == o.rows && cols == o.cols && ld == o.ld && box == o.box && kind == o.kind;
+    }
+};
+
+class MapCache {
+  public:
+    bool get(const MapKey& k, CUtensorMap* m) {
+        std::lock_guard<std::mutex> lock(mu_);
+        for (int i = 0; i < kSize; ++i)
+            if (used_[i] && keys_[i] == k) {
+                *m = maps_[i];
+                return true;
+            }
+        return false;
+    }
+    void put(const MapKey& k, const CUtensorMap& m) {
+        std::lock_guard<std::mutex> lock(mu_);
+        keys_[next_] = k;
+        maps_[next_] = m;
+        used_[next_] = true;
+        next_ = (next_ + 1) % kSize;
+    }
+
+  private:
+    static constexpr int kSize = 64;
+    std::mutex mu_;
+    MapKey keys_[kSize] = {};
+    CUtensorMap maps_[kSize] = {};
+    bool used_[kSize] = {};
+    int next_ = 0;
+};
+
+MapCache& map_cache() {
+    static MapCache c;
+    return c;
+}
+
+bool cached_map(CUtensorMap* m, const void* base, int64_t rows, int64_t K, int64_t ld, int box_rows) {
+    const MapKey k{base, rows, K, ld, box_rows, 0};
+    if (map_cache().get(k, m)) return true;
+    if (!make_map(m, base, rows, K, ld, box_rows)) return false;
+    map_cache().put(k, *m);
+    return true;
+}
+
+bool cached_out_map(CUtensorMap* m, void* base, int64_t rows, int64_t cols, int64_t ld, int box_cols) {
+    const MapKey k{base, rows, cols, ld, box_cols, 1};
+    if (map_cache().get(k, m)) return true;
+    if (!make_out_map(m, base, rows, cols, ld, box_cols)) return false;
+    map_cache().put(k, *m);
+    return true;
+}
+
+// cudaFuncSetAttribute once per (kernel, device, size): it is host work on
+// every call otherwise.
+bool set_smem_attr(const void* kern, size_t smem) {
+    static std::mutex mu;
+    static std::vector<std::tuple<const void*, int, size_t>> done;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    for (const auto& d : done)
+        if (std::get<0>(d) == kern && std::get<1>(d) == dev && std::get<2>(d) >= smem) return true;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    done.emplace_back(kern, dev, smem);
+    return true;
 }
 
 std::atomic<uint32_t> g_inject{0};
@@ -1415,11 +1500,7 @@ dsnq_status launch(gemm::Params& prm, const CUtensorMap& ma, const CUtensorMap& 
     auto kern = gemm::block_scaled_gemm_kernel<BN, SWAP, STAGES, NBUF, EPI_WARPS>;
     const size_t smem = gemm::smem_bytes<BN, SWAP, STAGES, NBUF, EPI_WARPS>(prm.KB);
     if (smem > 227 * 1024) return DSNQ_ERR_UNSUPPORTED;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
-        cudaSuccess) {
-        cudaGetLastError();
-        return DSNQ_ERR_CUDA;
-    }
+    if (!set_smem_attr(reinterpret_cast<const void*>(kern), smem)) return DSNQ_ERR_CUDA;
     // Persistent: one CTA per SM (the shared-memory ring allows one), each
     // walking the tile space with a stride of the grid size.
     const int sms = device_sm_count();
@@ -1435,11 +1516,7 @@ dsnq_status launch_pair(gemm::Params& prm, const CUtensorMap& ma, const CUtensor
     const size_t smem = gemm::pair::smem_bytes(prm.KB);
     if (smem > 227 * 1024) return DSNQ_ERR_UNSUPPORTED;
     auto kern = gemm::pair_gemm_kernel;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
-        cudaSuccess) {
-        cudaGetLastError();
-        return DSNQ_ERR_CUDA;
-    }
+    if (!set_smem_attr(reinterpret_cast<const void*>(kern), smem)) return DSNQ_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1514,7 +1591,7 @@ dsnq_status run_gemm(int64_t M, int64_t K, const void* a, int64_t lda, const flo
     prm.tiles_m = static_cast<int>((M + rows_per_a_tile - 1) / rows_per_a_tile);
 
     CUtensorMap ma, mw[2], mo[2];
-    if (!make_map(&ma, a, M, K, lda, a_box)) return DSNQ_ERR_CUDA;
+    if (!cached_map(&ma, a, M, K, lda, a_box)) return DSNQ_ERR_CUDA;
     const Consumer* cs[2] = {&c0, &c1};
     int64_t total = 0, total_super = 0;
     int np = 0;
@@ -1530,8 +1607,8 @@ dsnq_status run_gemm(int64_t M, int64_t K, const void* a, int64_t lda, const flo
         pr.ld_ws = c.ldws;
         pr.out = static_cast<__nv_bfloat16*>(c.out);
         pr.ldo = c.ldo;
-        if (!make_map(&mw[np], c.w, c.N, K, c.ldw, w_box)) return DSNQ_ERR_CUDA;
-        if (!swap && !make_out_map(&mo[np], c.out, M, c.N, c.ldo, paired ? 64 : 32)) return DSNQ_ERR_CUDA;
+        if (!cached_map(&mw[np], c.w, c.N, K, c.ldw, w_box)) return DSNQ_ERR_CUDA;
+        if (!swap && !cached_out_map(&mo[np], c.out, M, c.N, c.ldo, paired ? 64 : 32)) return DSNQ_ERR_CUDA;
         const int64_t tiles = static_cast<int64_t>(prm.tiles_m) * pr.tiles_n;
         const int64_t supers = static_cast<int64_t>(prm.tiles_m2) * ((c.N + 255) / 256);
         if (np == 0) {
