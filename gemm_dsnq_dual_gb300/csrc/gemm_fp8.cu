@@ -561,15 +561,27 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
             uint8_t* st = tiles + s * C::kStageBytes;
             uint32_t last = 0;     // 1 + the last K block this lane issued (0: none)
             bool ok = true;
+            // The lanes wait on different barriers and so run apart: the (tile,
+            // K block) position advances incrementally and the tile's
+            // coordinates are recomputed only when the tile changes.
+            int tl = s / KB, kbn = s % KB, cur_tl = -1;
+            int pi = 0, m0 = 0, n0 = 0;
             for (uint32_t g = s; g < ng; g += STAGES) {
                 if (!wait_bounded(smem_u32(&empty[s]), ((g / STAGES) & 1) ^ 1, abort_flag, tmo)) {
                     ok = false;
                     break;
                 }
+                if (tl != cur_tl) {
+                    tile_coords<BN, SWAP>(p, blockIdx.x + tl * gridDim.x, pi, m0, n0);
+                    cur_tl = tl;
+                }
+                const int kb = kbn;
+                kbn += STAGES;
+                while (kbn >= KB) {
+                    kbn -= KB;
+                    ++tl;
+                }
                 if ((p.inject & 1u) && g == 0) continue;   // test hook: never arrive on full[0]
-                const int tl = static_cast<int>(g / KB), kb = static_cast<int>(g % KB);
-                int pi, m0, n0;
-                tile_coords<BN, SWAP>(p, blockIdx.x + tl * gridDim.x, pi, m0, n0);
                 const CUtensorMap* map_w = pi ? &map_w1 : &map_w0;
                 if (!loads_q) {
                     mbar_arrive_expect_tx(fb, C::kStageBytes);
@@ -1072,22 +1084,35 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
             uint8_t* st = tiles + s * kStageBytes;
             uint32_t last = 0;
             bool ok = true;
+            // The lanes of this warp wait on different barriers, so they run
+            // apart and each executes its own instructions: the (tile, K
+            // block) position advances incrementally and the tile's
+            // coordinates are recomputed only when the tile changes.
+            int tl = s / KB, kb = s % KB, cur_tl = -1;
+            int pi = 0, m0 = 0, n0 = 0;
             for (uint32_t g = s; g < ng; g += kStages) {
                 if (!wait_bounded(smem_u32(&empty[s]), ((g / kStages) & 1) ^ 1, abort_flag, tmo)) {
                     ok = false;
                     break;
                 }
+                if (tl != cur_tl) {
+                    coords(first + tl * stride, pi, m0, n0);
+                    cur_tl = tl;
+                }
+                const int kbi = kb;
+                kb += kStages;
+                while (kb >= KB) {
+                    kb -= KB;
+                    ++tl;
+                }
                 if ((p.inject & 1u) && g == 0) continue;   // test hook: never arrive on full[0]
-                const int tl = static_cast<int>(g / KB), kb = static_cast<int>(g % KB);
-                int pi, m0, n0;
-                coords(first + tl * stride, pi, m0, n0);
                 if (part == 0) {
                     if (even) mbar_arrive_expect_tx(smem_u32(&full[s]), 2 * kStageBytes);
-                    tma_load_2d_pair(smem_u32(st), &map_a, fb, kb * kBK, m0);
+                    tma_load_2d_pair(smem_u32(st), &map_a, fb, kbi * kBK, m0);
                 } else {
                     const int h = part - 1;
                     tma_load_2d_pair(smem_u32(st + kHalfBytes + h * (kHalfBytes / 2)), pi ? &map_w1 : &map_w0, fb,
-                                     kb * kBK, n0 + h * kHalfN + static_cast<int>(rank) * (kHalfN / 2));
+                                     kbi * kBK, n0 + h * kHalfN + static_cast<int>(rank) * (kHalfN / 2));
                 }
                 last = g + 1;
             }
