@@ -616,7 +616,7 @@ def main():
     ap.add_argument("--nq-sweep", type=int, nargs="*", default=[1024, 8192, 32768])
     ap.add_argument("--side-reps", type=int, default=20)
     ap.add_argument("--gemm-sweep", type=int, nargs="*", default=[1, 8, 64, 128, 1024])
-    ap.add_argument("--cpu-rows", type=int, default=2560)
+    ap.add_argument("--cpu-rows", type=int, default=12288)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--kernel-only", choices=["gemm", "norm_quant"], default=None,
                     help="profiling aid: launch one kernel --launches times and exit")

@@ -29,7 +29,7 @@ GROUP = 128
 
 __all__ = [
     "ROW_MAJOR", "COL_MAJOR", "DsnqError",
-    "fused_dual_rmsnorm_group_quant", "dual_rmsnorm_bf16", "group_quant_bf16",
+    "fused_dual_rmsnorm_group_quant", "rmsnorm_group_quant", "dual_rmsnorm_bf16", "group_quant_bf16",
     "quantize_weight_block128", "block_scaled_fp8_gemm", "block_scaled_fp8_gemm_dual",
     "quant_output_sizes", "debug_status", "debug_set", "scale_layout_of", "scale_ld_for", "empty_scales",
 ]
@@ -119,6 +119,24 @@ def fused_dual_rmsnorm_group_quant(q, kv, gamma_q, gamma_kv, eps: float = 1e-6, 
         kv_out.data_ptr(), _row_view_ok(kv_out, "kv_out"), _stream(stream)),
         "dsnq_fused_dual_rmsnorm_group_quant")
     return q_out, q_scale, kv_out
+
+
+def rmsnorm_group_quant(x, gamma, eps: float = 1e-6, group: int = GROUP, scale_layout=ROW_MAJOR,
+                        x_out=None, x_scale=None, stream=None):
+    """RMSNorm one latent x [M,K] (bf16, rows may be a strided view) and
+    quantize it per 1x128 group to E4M3FN.  Returns (x_fp8, x_scale)."""
+    M, K = x.shape
+    lay = _layout(scale_layout)
+    if x_out is None:
+        x_out = torch.empty(M, K, dtype=torch.float8_e4m3fn, device=x.device)
+    if x_scale is None:
+        x_scale = empty_scales(M, K // group, lay, x.device)
+    ld = scale_ld_for(x_scale, lay)
+    check(lib().dsnq_rmsnorm_group_quant(
+        M, K, x.data_ptr(), _row_view_ok(x, "x"), gamma.data_ptr(), float(eps), group,
+        x_out.data_ptr(), _row_view_ok(x_out, "x_out"), x_scale.data_ptr(), lay, ld, _stream(stream)),
+        "dsnq_rmsnorm_group_quant")
+    return x_out, x_scale
 
 
 def dual_rmsnorm_bf16(q, kv, gamma_q, gamma_kv, eps: float = 1e-6, q_out=None, kv_out=None, stream=None):

@@ -30,6 +30,7 @@ SIGNATURES = {
     "dsnq_fused_dual_rmsnorm_group_quant": (
         i32, [i64, i64, i64, vp, i64, vp, i64, vp, vp, f32, i32,
               vp, i64, vp, i32, i64, vp, i64, vp]),
+    "dsnq_rmsnorm_group_quant": (i32, [i64, i64, vp, i64, vp, f32, i32, vp, i64, vp, i32, i64, vp]),
     "dsnq_dual_rmsnorm_bf16": (
         i32, [i64, i64, i64, vp, i64, vp, i64, vp, vp, f32, vp, i64, vp, i64, vp]),
     "dsnq_group_quant_bf16": (i32, [i64, i64, vp, i64, i32, vp, i64, vp, i32, i64, vp]),

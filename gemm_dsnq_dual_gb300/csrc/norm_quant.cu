@@ -731,6 +731,40 @@ extern "C" dsnq_status dsnq_fused_dual_rmsnorm_group_quant(
     return launch_rows<kFused>(a, M, static_cast<cudaStream_t>(stream));
 }
 
+extern "C" dsnq_status dsnq_rmsnorm_group_quant(
+    int64_t M, int64_t K, const void* x, int64_t ldx, const void* gamma, float eps, int32_t group,
+    void* x_fp8, int64_t ldx_out, float* x_scale, dsnq_scale_layout layout, int64_t ld_scale, void* stream) {
+    if (M < 0 || K <= 0) return DSNQ_ERR_INVALID_ARG;
+    if (!(eps >= 0.f) || eps > 3.0e38f) return DSNQ_ERR_INVALID_ARG;   // also rejects NaN
+    if (layout != DSNQ_SCALE_ROW_MAJOR && layout != DSNQ_SCALE_COL_MAJOR) return DSNQ_ERR_INVALID_ARG;
+    if (group != 128 || K % 128 != 0 || K / 8 > 4 * kThreads || M > 0x7fffffffLL) return DSNQ_ERR_UNSUPPORTED;
+    if (M == 0) return DSNQ_OK;
+    if (!x || !gamma || !x_fp8 || !x_scale) return DSNQ_ERR_INVALID_ARG;
+    if (ldx < K || ldx_out < K) return DSNQ_ERR_INVALID_ARG;
+    const int64_t ld = scale_ld(layout, M, K / 128, ld_scale);
+    if (ld < 0) return DSNQ_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(gamma, 16) || ldx % 8 || !aligned(x_fp8, 8) || ldx_out % 8 ||
+        !aligned(x_scale, 4))
+        return DSNQ_ERR_MISALIGNED;
+    // The fused kernels with an empty kv part (no kv chunk is ever touched).
+    RowArgs a{};
+    a.q = static_cast<const __nv_bfloat16*>(x);
+    a.kv = a.q;
+    a.gamma_q = static_cast<const __nv_bfloat16*>(gamma);
+    a.gamma_kv = a.gamma_q;
+    a.ldq = ldx; a.ldkv = ldx;
+    a.cq = static_cast<int>(K / 8); a.ckv = 0;
+    a.kq_f = static_cast<float>(K); a.kkv_f = 1.0f;
+    a.eps = eps;
+    a.q_fp8 = static_cast<uint8_t*>(x_fp8);
+    a.ldq_out = ldx_out;
+    a.scale = x_scale;
+    set_scale_strides(a, layout, ld);
+    a.kv_out = nullptr;
+    a.ldkv_out = 0;
+    return launch_rows<kFused>(a, M, static_cast<cudaStream_t>(stream));
+}
+
 extern "C" dsnq_status dsnq_dual_rmsnorm_bf16(
     int64_t M, int64_t Kq, int64_t Kkv,
     const void* q, int64_t ldq, const void* kv, int64_t ldkv,

@@ -99,7 +99,8 @@ DSNQ_API dsnq_status dsnq_quant_output_sizes(int64_t M, int64_t Kq, int32_t grou
  *   xq   = q * r_q * gamma_q,  xkv = kv * r_kv * gamma_kv   (fp32)
  *   per group g of 128 columns of xq: amax = max |xq|,
  *     q_scale(m, g) = amax / 448  (fp32; 0 when amax == 0),
- *     q_fp8[m, k]   = e4m3_rn_satfinite(xq[m,k] * 448 / amax)  (0 when amax == 0)
+ *     q_fp8[m, k]   = e4m3_rn_satfinite(fp32(xq[m,k] / q_scale(m, g)))  (0 when amax == 0),
+ *                     the quotient taken on the fp32 values (single rounding)
  *   kv_out[m, k]  = bf16_rn(xkv[m, k])
  * One eps serves both latents (the model passes the same self.eps to both).
  *
@@ -133,6 +134,26 @@ DSNQ_API dsnq_status dsnq_fused_dual_rmsnorm_group_quant(
     void* q_fp8, int64_t ldq_out,
     float* q_scale, dsnq_scale_layout layout, int64_t ld_scale,
     void* kv_out, int64_t ldkv_out,
+    void* stream);
+
+/*
+ * Single-latent RMSNorm + per-1x128 FP8 group quant: the fused call for one
+ * latent, as in the DeepSeek MLA pattern that normalizes one latent before
+ * its block-scaled FP8 projection (sglang PR #27289, fused_rms_fp8_group_quant
+ * with transpose_scale).  Same formulas as the q part of the fused call:
+ *   r = 1 / sqrt(mean_k x[m,k]^2 + eps),  xn = x * r * gamma  (fp32),
+ *   x_scale(m, g) = amax_g / 448,  x_fp8 = e4m3_rn_satfinite(fp32(xn / x_scale)).
+ * Arguments: M rows; K (multiple of 128, <= 4096); x bf16 [M, K] with row
+ * stride ldx (multiple of 8, may be a column slice of a wider buffer);
+ * gamma bf16 [K]; eps, group, x_fp8/ldx_out, x_scale/layout/ld_scale as in
+ * the fused call.  Alignment and error rules as in the fused call.
+ */
+DSNQ_API dsnq_status dsnq_rmsnorm_group_quant(
+    int64_t M, int64_t K,
+    const void* x, int64_t ldx, const void* gamma,
+    float eps, int32_t group,
+    void* x_fp8, int64_t ldx_out,
+    float* x_scale, dsnq_scale_layout layout, int64_t ld_scale,
     void* stream);
 
 /*

@@ -213,6 +213,15 @@ def fused_dual_rmsnorm_group_quant(q_bits, kv_bits, gamma_q_bits, gamma_kv_bits,
     return codes, scale, f64_to_bf16_bits(xkv)
 
 
+def rmsnorm_group_quant(x_bits, gamma_bits, eps: float, group: int = GROUP):
+    """Single-latent RMSNorm + per-1x128 group quant (sglang PR #27289,
+    fused_rms_fp8_group_quant): the q part of the fused op for one latent.
+    Returns (codes uint8 [M,K], scale float32 [M,K/group] logical)."""
+    eps = float(np.float32(eps))
+    x = rmsnorm_f64(bf16_bits_to_f64(x_bits), bf16_bits_to_f64(gamma_bits), eps)
+    return group_quant_f64(x, group)
+
+
 def normalized_latents(q_bits, kv_bits, gamma_q_bits, gamma_kv_bits, eps: float):
     """The unrounded fp64 normalized latents (x_hat_q, x_hat_kv)."""
     eps = float(np.float32(eps))

@@ -125,6 +125,20 @@ def test_dual_and_helpers_argument_checks(lib):
     assert lib.dsnq_dual_rmsnorm_bf16(0, 1536, 512, A, 1536, A, 512, A, A, 1e-6, A, 1536, A, 512, None) == OK
 
 
+def test_single_latent_argument_checks(lib):
+    f = lib.dsnq_rmsnorm_group_quant
+    assert f(0, 1536, None, 1536, None, 1e-6, 128, None, 1536, None, 0, 0, None) == OK     # empty call
+    assert f(4, 1536, A, 1536, A, 1e-6, 64, A, 1536, A, 0, 0, None) == UNSUPPORTED        # group
+    assert f(4, 1500, A, 1536, A, 1e-6, 128, A, 1536, A, 0, 0, None) == UNSUPPORTED       # K % 128
+    assert f(4, 8192, A, 8192, A, 1e-6, 128, A, 8192, A, 0, 0, None) == UNSUPPORTED       # K > 4096
+    assert f(4, 1536, A, 1000, A, 1e-6, 128, A, 1536, A, 0, 0, None) == INVALID           # ldx < K
+    assert f(4, 1536, A, 1536, A, float("nan"), 128, A, 1536, A, 0, 0, None) == INVALID   # eps
+    assert f(4, 1536, A + 8, 1536, A, 1e-6, 128, A, 1536, A, 0, 0, None) == MISALIGNED    # x
+    assert f(4, 1536, A, 1540, A, 1e-6, 128, A, 1536, A, 0, 0, None) == MISALIGNED        # ldx
+    assert f(4, 1536, A, 1536, A, 1e-6, 128, A, 1536, A, 1, 2, None) == INVALID           # col-major ld < M
+    assert f(4, 1536, None, 1536, A, 1e-6, 128, A, 1536, A, 0, 0, None) == INVALID        # null x
+
+
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(_native, "_lib", None)
     monkeypatch.setattr(_native, "LIB_PATH", str(tmp_path / "libdsnq.so"))

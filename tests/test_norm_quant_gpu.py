@@ -219,3 +219,29 @@ def test_weight_block_quantizer():
     wc, ws = oracle.quantize_weight_block128(w.numpy())
     assert_scales_close(sw.cpu().numpy(), ws)
     assert_codes_close(u8(codes), wc)
+
+
+# ------------------------------------------------------- single-latent variant
+
+@pytest.mark.parametrize("M,K", [(1, 1536), (5, 512), (300, 2048), (2048, 1536), (4, 4096)])
+@pytest.mark.parametrize("layout", [dsnq.ROW_MAJOR, dsnq.COL_MAJOR])
+def test_single_latent_rmsnorm_group_quant(M, K, layout):
+    g = torch.Generator().manual_seed(M + K)
+    buf = (torch.randn(M, K + 64, generator=g) * 2.0).to(torch.bfloat16)     # rows of a wider buffer
+    x = buf[:, :K]
+    gamma = (torch.rand(K, generator=g) + 0.5).to(torch.bfloat16)
+    codes, scale = dsnq.rmsnorm_group_quant(buf.cuda()[:, :K], gamma.cuda(), 1e-6, scale_layout=layout)
+    wc, ws = oracle.rmsnorm_group_quant(inputs.bits(x.contiguous()), inputs.bits(gamma), 1e-6)
+    assert_scales_close(scale.cpu().numpy(), ws)
+    assert_codes_close(u8(codes), wc)
+
+
+def test_single_latent_zero_rows_and_matches_fused_q_part():
+    lat = inputs.decode_batch(16, seed=12)
+    q, kv = to_device(lat)
+    gq, gkv = lat.gamma_q.cuda(), lat.gamma_kv.cuda()
+    c1, s1 = dsnq.rmsnorm_group_quant(q, gq, lat.eps)
+    c2, s2, _ = dsnq.fused_dual_rmsnorm_group_quant(q, kv, gq, gkv, lat.eps)
+    assert torch.equal(c1.view(torch.uint8), c2.view(torch.uint8)) and torch.equal(s1, s2)
+    e = torch.empty(0, 1536, dtype=torch.bfloat16, device="cuda")
+    assert dsnq.rmsnorm_group_quant(e, gq, 1e-6)[0].shape == (0, 1536)

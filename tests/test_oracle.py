@@ -274,3 +274,21 @@ def test_gemm_bruteforce_triple_loop():
                     part += dec_a[m, k] * dec_w[n, k]
                 acc += float(sa[m, kb]) * float(sw[n // 128, kb]) * part
             assert abs(acc - got[m, n]) <= 1e-12 * max(1.0, abs(acc))
+
+
+def test_single_latent_is_the_q_part_of_the_fused_op():
+    """The single-latent op is the fused op's q computation on its own: same
+    codes and scales for the same latent, whatever the kv latent is."""
+    rng = np.random.default_rng(11)
+    q = oracle.f64_to_bf16_bits(rng.standard_normal((6, 512)) * 3.0)
+    kv = oracle.f64_to_bf16_bits(rng.standard_normal((6, 64)))
+    gq = oracle.f64_to_bf16_bits(rng.uniform(0.5, 1.5, 512))
+    gkv = oracle.f64_to_bf16_bits(rng.uniform(0.5, 1.5, 64))
+    c1, s1 = oracle.rmsnorm_group_quant(q, gq, 1e-6)
+    c2, s2, _ = oracle.fused_dual_rmsnorm_group_quant(q, kv, gq, gkv, 1e-6)
+    assert np.array_equal(c1, c2) and np.array_equal(s1, s2)
+    # constant row: every code is +-448 and the scale is |x_hat| / 448
+    const = oracle.f64_to_bf16_bits(np.full((1, 256), 2.0))
+    ones = oracle.f64_to_bf16_bits(np.ones(256))
+    c, s = oracle.rmsnorm_group_quant(const, ones, 0.0)
+    assert np.all(c == 0x7E) and np.allclose(s, np.float32(1.0) / np.float32(448.0))
