@@ -611,7 +611,15 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                 for (int kb = 0; kb < KB; ++kb, ++g) {
                     const int s = g % STAGES;
                     const int b = g % NBUF;
-                    if (g >= ready && !wait_gate(smem_u32(gate), g, ready, abort_flag, tmo)) {
+                    if (SWAP) {
+                        // Decode: the tensor core idles most of the time, so the
+                        // MMA warp waits on the barriers itself (no gate hop).
+                        if (!wait_bounded<true>(smem_u32(&full[s]), (g / STAGES) & 1, abort_flag, tmo) ||
+                            !wait_bounded<true>(smem_u32(&tempty[b]), ((g / NBUF) & 1) ^ 1, abort_flag, tmo)) {
+                            ok = false;
+                            break;
+                        }
+                    } else if (g >= ready && !wait_gate(smem_u32(gate), g, ready, abort_flag, tmo)) {
                         ok = false;
                         break;
                     }
@@ -635,8 +643,8 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
         }
         __syncwarp();
     } else if (warp == 2) {
-        // ------------------------------------------------ gate (one lane)
-        if (lane == 0) {
+        // ------------------------------------------------ gate (one lane; not used for decode)
+        if (!SWAP && lane == 0) {
             uint32_t g = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
