@@ -477,6 +477,8 @@ def _sample_inputs(rows, cols_per_consumer, seed, M):
         import oracle
         from gemm_dsnq_dual_gb300 import inputs
         lat = inputs.full_path_batch(M, seed=seed)
+        if rows > M:
+            raise ValueError(f"a sample of {rows} rows does not fit the M={M} workload")
         pick = np.random.default_rng(0).choice(M, rows, replace=False)
         b = [inputs.bits(t) for t in (lat.q[pick], lat.kv[pick], lat.gamma_q, lat.gamma_kv)]
         weights = []
@@ -616,7 +618,7 @@ def main():
     ap.add_argument("--nq-sweep", type=int, nargs="*", default=[1024, 8192, 32768])
     ap.add_argument("--side-reps", type=int, default=20)
     ap.add_argument("--gemm-sweep", type=int, nargs="*", default=[1, 8, 64, 128, 1024])
-    ap.add_argument("--cpu-rows", type=int, default=12288)
+    ap.add_argument("--cpu-rows", type=int, default=4096)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--kernel-only", choices=["gemm", "norm_quant"], default=None,
                     help="profiling aid: launch one kernel --launches times and exit")

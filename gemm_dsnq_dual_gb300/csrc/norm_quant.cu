@@ -437,14 +437,16 @@ __device__ __forceinline__ uint2 quant8_bracket(const float2 (&f)[4], const Grou
 // Fused warp-per-row kernel for rows whose q and kv parts are whole warp
 // slots (Kq and Kkv multiples of 256: QS slots of q, KS of kv; DSv4: 6 + 2).
 //   * each slot's role is known at compile time (no per-chunk predicates);
-//   * the next row of the warp is loaded into registers while the current
-//     one is processed;
+//   * the next row of the warp is loaded into registers as soon as the
+//     current one is unpacked, and the row after it is prefetched into L2;
+//   * 4 CTAs of 4 warps per SM (128 registers): the kernel is bound by its
+//     instruction latency, so warps in flight matter more than ILP per warp;
 //   * the row is processed in phases over all slots (sums of squares, norm,
 //     group amax, scales, codes) so that the independent chains overlap;
 //   * the quantize step uses bracket reciprocals scaled once per group and
 //     takes the exactness decision for the whole row with one warp vote.
 // ---------------------------------------------------------------------------
-constexpr int kFusedCtasPerSM = 3;  // register budget: 168 per thread
+constexpr int kFusedCtasPerSM = 4;  // register budget: 128 per thread
 
 template <int QS, int KS>
 __global__ void __launch_bounds__(kRowWarps * 32, kFusedCtasPerSM)
@@ -478,13 +480,18 @@ warp_row_fused_kernel(const RowArgs a) {
     }
     __syncthreads();
 
+    auto prefetch_l2 = [&](int64_t mp) {      // lane l: 128-byte line l of row mp (q: 24 lines, kv: 8)
+        const char* p = lane < 24 ? reinterpret_cast<const char*>(a.q + mp * a.ldq) + lane * 128
+                                  : reinterpret_cast<const char*>(a.kv + mp * a.ldkv) + (lane - 24) * 128;
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+    };
+    if (m + stride < a.M) prefetch_l2(m + stride);
     for (; m < a.M; m += stride) {
-        uint4 nxt[CPT];
-        const int64_t mn = m + stride;
-        if (mn < a.M) load_row(mn, nxt);         // prefetch this warp's next row
+        if (m + 2 * stride < a.M) prefetch_l2(m + 2 * stride);
         float2 x[CPT][4];
 #pragma unroll
         for (int j = 0; j < CPT; ++j) unpack8(cur[j], x[j]);
+        if (m + stride < a.M) load_row(m + stride, cur);   // next row (in L2 by now), in flight meanwhile
         float2 sq[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
         float2 skv[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
@@ -528,43 +535,45 @@ warp_row_fused_kernel(const RowArgs a) {
             for (int j = 0; j < QS; ++j) am[j] = fmaxf(am[j], __shfl_xor_sync(0xffffffffu, am[j], o));
         }
 
-        // Scales and codes.
-        GroupQuant gq[QS];
-        uint2 codes[QS];
-        bool ok_all = true;
+        // Scales and codes, three q slots at a time (fewer live registers).
+        constexpr int kGrp = 3;
+        static_assert(QS % kGrp == 0, "q slots in groups of three");
 #pragma unroll
-        for (int j = 0; j < QS; ++j) {
-            gq[j] = make_group_quant(am[j]);
-            bool ok;
-            codes[j] = quant8_bracket(x[j], gq[j], ok);
-            ok_all = ok_all && ok;
-        }
-        if (!__all_sync(0xffffffffu, ok_all)) {
-            // Rare: a code within 2^-20 of a rounding boundary, or a scale
-            // that is zero or too small for a reciprocal: the division itself
-            // (x * 0 keeps the sign of zero codes of a zero group).
+        for (int j0 = 0; j0 < QS; j0 += kGrp) {
+            GroupQuant gq[kGrp];
+            uint2 codes[kGrp];
+            bool ok_all = true;
 #pragma unroll
-            for (int j = 0; j < QS; ++j) {
+            for (int u = 0; u < kGrp; ++u) {
+                gq[u] = make_group_quant(am[j0 + u]);
                 bool ok;
-                quant8_bracket(x[j], gq[j], ok);
-                if (ok) continue;
-                const float sc = gq[j].scale;
-                float2 qv[4];
+                codes[u] = quant8_bracket(x[j0 + u], gq[u], ok);
+                ok_all = ok_all && ok;
+            }
+            if (!__all_sync(0xffffffffu, ok_all)) {
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    qv[i] = sc > 0.f ? make_float2(__fdiv_rn(x[j][i].x, sc), __fdiv_rn(x[j][i].y, sc))
-                                     : make_float2(x[j][i].x * 0.f, x[j][i].y * 0.f);
-                codes[j] = make_uint2(e4m3x2(qv[0]) | (e4m3x2(qv[1]) << 16), e4m3x2(qv[2]) | (e4m3x2(qv[3]) << 16));
+                for (int u = 0; u < kGrp; ++u) {
+                    bool ok;
+                    quant8_bracket(x[j0 + u], gq[u], ok);
+                    if (ok) continue;
+                    const float sc = gq[u].scale;
+                    float2 qv[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        qv[i] = sc > 0.f ? make_float2(__fdiv_rn(x[j0 + u][i].x, sc), __fdiv_rn(x[j0 + u][i].y, sc))
+                                         : make_float2(x[j0 + u][i].x * 0.f, x[j0 + u][i].y * 0.f);
+                    codes[u] = make_uint2(e4m3x2(qv[0]) | (e4m3x2(qv[1]) << 16), e4m3x2(qv[2]) | (e4m3x2(qv[3]) << 16));
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kGrp; ++u) {
+                const int col = (j0 + u) * 256 + lane * kChunk;
+                *reinterpret_cast<uint2*>(a.q_fp8 + m * a.ldq_out + col) = codes[u];
+                if ((lane & 15) == 0)
+                    a.scale[m * a.scale_row_stride + (col / 128) * a.scale_group_stride] = gq[u].scale;
             }
         }
-#pragma unroll
-        for (int j = 0; j < QS; ++j) {
-            const int col = j * 256 + lane * kChunk;
-            *reinterpret_cast<uint2*>(a.q_fp8 + m * a.ldq_out + col) = codes[j];
-            if ((lane & 15) == 0) a.scale[m * a.scale_row_stride + (col / 128) * a.scale_group_stride] = gq[j].scale;
-        }
-    #pragma unroll
-        for (int j = 0; j < CPT; ++j) cur[j] = nxt[j];
+
     }
 }
 
