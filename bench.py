@@ -521,7 +521,8 @@ def cpu_baseline(rows: int):
     secs, flops = oracle_full_path_sample(rows, None)
     return {"value": round(flops / secs / 1e12, 6), "unit": "TFLOP/s", "cores": blas_threads(),
             "kind": "oracle",
-            "sample": f"{rows} random rows of the M=8192 full path: fp64 norm+quant, then the dequantize-"
+            "sample": ("all 8192 rows" if rows == 8192 else f"{rows} random rows") + " of the M=8192 full path: "
+                      f"fp64 norm+quant, then the dequantize-"
                       f"then-fp64 GEMM against all 24576+4096 features ({secs:.1f} s)"}
 
 
@@ -618,7 +619,7 @@ def main():
     ap.add_argument("--nq-sweep", type=int, nargs="*", default=[1024, 8192, 32768])
     ap.add_argument("--side-reps", type=int, default=20)
     ap.add_argument("--gemm-sweep", type=int, nargs="*", default=[1, 8, 64, 128, 1024])
-    ap.add_argument("--cpu-rows", type=int, default=4096)
+    ap.add_argument("--cpu-rows", type=int, default=8192)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--kernel-only", choices=["gemm", "norm_quant"], default=None,
                     help="profiling aid: launch one kernel --launches times and exit")

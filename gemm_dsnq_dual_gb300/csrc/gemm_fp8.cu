@@ -21,14 +21,12 @@
 //     (tcgen05.ld), multiply by sa * sw and add it into fp32 registers while
 //     the MMAs of the next K blocks fill the other buffers.
 //   * Warp roles: warp 0 issues TMA, warp 1 allocates TMEM and issues MMA
-//     (the whole warp runs the loop, one elected lane issues), warp 2 is the
-//     gate, warp 3 loads the scales, warps 4.. promote and store.  A wait or
-//     shared-memory load in the MMA-issuing warp stalls it behind the MMAs
-//     already in flight (about 100 cycles each, measured on GB300), so the
-//     MMA warp performs almost none: the gate thread waits for "stage loaded"
-//     and "TMEM buffer free" and publishes a running count of K blocks ready,
-//     which the MMA warp re-reads only when it has caught up with its last
-//     reading.  Warp w may only read TMEM lanes
+//     (the whole warp runs the loop, one elected lane issues), warp 2 idles,
+//     warp 3 loads the scales, warps 4.. promote and store.  The MMA warp
+//     itself waits for "stage loaded" and "TMEM buffer free".  A separate gate
+//     thread that waited on those and published a count of ready K blocks
+//     measured slower on GB300 at every batch size: the extra hop lengthens
+//     the MMA -> promotion -> MMA round trip.  Warp w may only read TMEM lanes
 //     32*(w%4)..+31, so each group of four promotion warps covers all 128 lanes
 //     and the groups split the tile's columns.
 //   * Orientation.  The MMA's M side ("P", 128 rows) and N side ("Q", BN rows)
@@ -171,37 +169,6 @@ __device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, uint64
     const uint64_t t0 = now_ns();
     while (!mbar_try_wait_sleep(bar, parity, kSleepHintNs)) {
         if (now_ns() - t0 > timeout_ns) return;
-    }
-}
-
-__device__ __forceinline__ void st_release_shared(uint32_t addr, uint32_t v) {
-    asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
-}
-
-__device__ __forceinline__ uint32_t ld_acquire_shared(uint32_t addr) {
-    uint32_t v;
-    asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
-    return v;
-}
-
-// MMA thread: wait until the gate's count exceeds `need` (bounded like
-// wait_bounded); `ready` receives the count read.
-__device__ __forceinline__ bool wait_gate(uint32_t gate, uint32_t need, uint32_t& ready, volatile int* abort,
-                                          uint64_t timeout_ns) {
-    ready = ld_acquire_shared(gate);
-    if (ready > need) return true;
-    const uint64_t t0 = now_ns();
-    uint32_t n = 0;
-    while (true) {
-        ready = ld_acquire_shared(gate);
-        if (ready > need) return true;
-        if (++n & 63) continue;                  // check abort and the clock every 64 polls
-        if (*abort) return false;
-        if (now_ns() - t0 > timeout_ns) {
-            *abort = 1;
-            atomicOr(&g_status, kStatusTimeout);
-            return false;
-        }
     }
 }
 
@@ -451,7 +418,7 @@ struct Cfg {
     // (rows of kCols*2 = 64 bytes, 64-byte swizzle) for one TMA store.
     static constexpr int kStageOutBytes = SWAP ? 0 : 32 * kCols * 2;
     static_assert(SWAP || kCols == 32, "the store box is 32 rows x 64 bytes");
-    static constexpr int kThreads = (4 + EPI_WARPS) * 32;  // producer, MMA, gate, scale loader, promotion
+    static constexpr int kThreads = (4 + EPI_WARPS) * 32;  // producer, MMA, idle, scale loader, promotion
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M=128 is 16..256 step 16");
     static_assert(kTmemNeed <= 512, "TMEM holds 512 fp32 columns");
     static_assert(EPI_WARPS % 4 == 0 && BN % kSlices == 0, "promotion warps tile the accumulator");
@@ -489,13 +456,12 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
     uint64_t* full = bars;                    // [STAGES] TMA -> MMA
     uint64_t* empty = bars + STAGES;          // [STAGES] MMA -> TMA
     uint64_t* tfull = bars + 2 * STAGES;      // [NBUF]   MMA -> promotion
-    uint64_t* tempty = tfull + NBUF;          // [NBUF]   promotion -> gate
+    uint64_t* tempty = tfull + NBUF;          // [NBUF]   promotion -> MMA
     uint64_t* sfull = tempty + NBUF;          // [2]      scale loader -> promotion
     uint64_t* sempty = sfull + 2;             // [2]      promotion -> scale loader
     uint64_t* drain = sempty + 2;             // [1]      abort drain of MMAs
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
-    uint32_t* gate = tmem_holder + 2;         // K blocks ready for the MMA thread
     // Scale slots (16-byte aligned), K blocks padded to KBP = a multiple of 4:
     // [2][KBP][kScaleCols] raw activation scales (per P row for non-swap, per
     // token for swap), then [2][KBP] weight scales.
@@ -523,7 +489,6 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
         }
         mbar_init(smem_u32(drain), 1);
         *abort_flag = 0;
-        *gate = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         tma_prefetch_desc(&map_a);
         tma_prefetch_desc(&map_w0);
@@ -605,21 +570,14 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
             // address field (16-byte units), which stays below 2^14 for 227 KB.
             const uint64_t dp0 = smem_desc_k_sw128(smem_u32(tiles));
             const uint64_t dq0 = smem_desc_k_sw128(smem_u32(tiles + C::kPBytes));
-            uint32_t g = 0, ready = 0;
+            uint32_t g = 0;
             bool ok = true, any = false;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
                 for (int kb = 0; kb < KB; ++kb, ++g) {
                     const int s = g % STAGES;
                     const int b = g % NBUF;
-                    if (SWAP) {
-                        // Decode: the tensor core idles most of the time, so the
-                        // MMA warp waits on the barriers itself (no gate hop).
-                        if (!wait_bounded<true>(smem_u32(&full[s]), (g / STAGES) & 1, abort_flag, tmo) ||
-                            !wait_bounded<true>(smem_u32(&tempty[b]), ((g / NBUF) & 1) ^ 1, abort_flag, tmo)) {
-                            ok = false;
-                            break;
-                        }
-                    } else if (g >= ready && !wait_gate(smem_u32(gate), g, ready, abort_flag, tmo)) {
+                    if (!wait_bounded<true>(smem_u32(&full[s]), (g / STAGES) & 1, abort_flag, tmo) ||
+                        !wait_bounded<true>(smem_u32(&tempty[b]), ((g / NBUF) & 1) ^ 1, abort_flag, tmo)) {
                         ok = false;
                         break;
                     }
@@ -639,23 +597,6 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
             if (*abort_flag && any) {
                 tc_commit(smem_u32(drain));            // completes once every MMA above has
                 wait_drain(smem_u32(drain), 0, tmo);
-            }
-        }
-        __syncwarp();
-    } else if (warp == 2) {
-        // ------------------------------------------------ gate (one lane; not used for decode)
-        if (!SWAP && lane == 0) {
-            uint32_t g = 0;
-            bool ok = true;
-            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-                for (int kb = 0; kb < KB; ++kb, ++g) {
-                    if (!wait_bounded<true>(smem_u32(&full[g % STAGES]), (g / STAGES) & 1, abort_flag, tmo) ||
-                        !wait_bounded<true>(smem_u32(&tempty[g % NBUF]), ((g / NBUF) & 1) ^ 1, abort_flag, tmo)) {
-                        ok = false;
-                        break;
-                    }
-                    st_release_shared(smem_u32(gate), g + 1);
-                }
             }
         }
         __syncwarp();
@@ -706,7 +647,7 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                          : "memory");
         }
         asm volatile("cp.async.wait_all;" ::: "memory");   // no copy outlives the CTA
-    } else {
+    } else if (warp >= 4) {
         // ------------------------------------------------ promotion + store
         const int ew = warp - 4;                 // 0 .. EPI_WARPS-1
         const int quarter = warp & 3;            // TMEM lanes 32*quarter .. +31
@@ -888,8 +829,8 @@ constexpr size_t smem_bytes(int KB) {
 // 128 x 128 tiles need at the full MMA rate, and more than the 64 B/clock
 // these tiles need.
 //
-// Roles as in block_scaled_gemm_kernel; the MMA warp and the gate run in the
-// even CTA only.  Both CTAs' loads signal the even CTA's stage barrier
+// Roles as in block_scaled_gemm_kernel; the MMA warp runs in the even CTA
+// only.  Both CTAs' loads signal the even CTA's stage barrier
 // (TMA .cta_group::2); the MMA completions are multicast to both CTAs'
 // "stage free" and "partial ready" barriers; both CTAs' promotion warps
 // release a TMEM buffer on the even CTA's barrier.  Each promotion thread
@@ -1015,13 +956,12 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
     uint64_t* full = bars;                    // [S]  even CTA: both CTAs' loads of a stage
     uint64_t* empty = bars + kStages;         // [S]  MMA -> TMA (multicast to both)
     uint64_t* tfull = bars + 2 * kStages;     // [2 halves][NB] MMA -> promotion (multicast to both)
-    uint64_t* tempty = tfull + 2 * kNBuf;     // [2 halves][NB] even CTA: both CTAs' promotion -> gate
+    uint64_t* tempty = tfull + 2 * kNBuf;     // [2 halves][NB] even CTA: both CTAs' promotion -> MMA
     uint64_t* sfull = tempty + 2 * kNBuf;     // [2]
     uint64_t* sempty = sfull + 2;             // [2]
     uint64_t* drain = sempty + 2;             // [1]
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
-    uint32_t* gate = tmem_holder + 2;
     const int KBP = (p.KB + 3) & ~3;
     float* sa_slots = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(tmem_holder + 8) + 15) & ~uintptr_t(15));
     float* sw_slots = sa_slots + 2 * KBP * kPRows;     // [2][2 blocks][KBP]
@@ -1057,7 +997,6 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
         }
         mbar_init(smem_u32(drain), 1);
         *abort_flag = 0;
-        *gate = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         tma_prefetch_desc(&map_a);
         tma_prefetch_desc(&map_w0);
@@ -1138,10 +1077,8 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
             constexpr uint32_t idesc = idesc_e4m3_pair();
             const uint64_t da0 = smem_desc_k_sw128(smem_u32(tiles));
             const uint64_t dw0 = smem_desc_k_sw128(smem_u32(tiles + kHalfBytes));
-            uint32_t g = 0, ready = 0;
+            uint32_t g = 0;
             bool ok = true, any = false;
-            // The gate counts column halves: half h of K block g may be issued
-            // once the count exceeds 2g + h.
             for (int it = 0; it < items && ok; ++it) {
                 for (int kb = 0; kb < KB && ok; ++kb, ++g) {
                     const int s = g % kStages;
@@ -1149,8 +1086,9 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
                     const uint64_t so = static_cast<uint64_t>((s * kStageBytes) >> 4);
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
-                        const uint32_t need = 2 * g + h;
-                        if (need >= ready && !wait_gate(smem_u32(gate), need, ready, abort_flag, tmo)) {
+                        if ((h == 0 && !wait_bounded<true>(smem_u32(&full[s]), (g / kStages) & 1, abort_flag, tmo)) ||
+                            !wait_bounded<true>(smem_u32(&tempty[h * kNBuf + q]), ((g / kNBuf) & 1) ^ 1, abort_flag,
+                                                tmo)) {
                             ok = false;
                             break;
                         }
@@ -1171,29 +1109,6 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
             if (*abort_flag && any) {
                 tc_commit_pair_local(smem_u32(drain));
                 wait_drain(smem_u32(drain), 0, tmo);
-            }
-        }
-        __syncwarp();
-    } else if (warp == 2) {
-        // ------------------------------------------------ gate (even CTA, one lane)
-        if (even && lane == 0) {
-            uint32_t g = 0;
-            bool ok = true;
-            for (int it = 0; it < items && ok; ++it) {
-                for (int kb = 0; kb < KB; ++kb, ++g) {
-                    const uint32_t q = g % kNBuf, par = ((g / kNBuf) & 1) ^ 1;
-                    if (!wait_bounded<true>(smem_u32(&full[g % kStages]), (g / kStages) & 1, abort_flag, tmo) ||
-                        !wait_bounded<true>(smem_u32(&tempty[q]), par, abort_flag, tmo)) {
-                        ok = false;
-                        break;
-                    }
-                    st_release_shared(smem_u32(gate), 2 * g + 1);
-                    if (!wait_bounded<true>(smem_u32(&tempty[kNBuf + q]), par, abort_flag, tmo)) {
-                        ok = false;
-                        break;
-                    }
-                    st_release_shared(smem_u32(gate), 2 * g + 2);
-                }
             }
         }
         __syncwarp();
