@@ -316,7 +316,12 @@ def side_measurements(torch, dsnq, inputs, dev, flush, hbm_gbs, args):
         buf[r:r + 1, :KQ], buf[r:r + 1, KQ:KQ + KKV], gq, gkv, dec.eps, q_out=qo, q_scale=so, kv_out=ko))
         for r in range(n)]
     out["norm_quant_us_at_M1"] = round(timed_graph_calls(torch, stream, calls, flush), 3)
-    out["norm_quant_us_at_M1_note"] = "per call, CUDA graph of 100 calls on 100 distinct cold rows, L2 flushed per replay"
+    dsnq.set_launch_overlap(False)
+    out["norm_quant_us_at_M1_no_overlap"] = round(timed_graph_calls(torch, stream, calls, flush), 3)
+    dsnq.set_launch_overlap(True)
+    out["norm_quant_us_at_M1_note"] = ("per call, CUDA graph of 100 calls on 100 distinct cold rows, L2 flushed per "
+                                       "replay; _no_overlap: the same with programmatic dependent launch off")
+    out["decode_step_us_at_M1"] = decode_step(torch, dsnq, inputs, dev, flush, buf, gq, gkv, dec.eps, qo, so, ko)
     out["gemm_sweep"] = gemm_sweep(torch, dsnq, inputs, dev, flush, hbm_gbs, args)
 
     # -- norm+quant GB/s over M, and the unfused three-kernel sequence at the same M
@@ -369,6 +374,33 @@ def side_measurements(torch, dsnq, inputs, dev, flush, hbm_gbs, args):
                                     "back-to-back calls over graph_sets distinct input/output sets (> 160 MiB in "
                                     "total, more than L2); M=8192 uses the prefill Student-t inputs, column-major scales")
     return out
+
+
+def decode_step(torch, dsnq, inputs, dev, flush, buf, gq, gkv, eps, qo, so, ko):
+    """One decode step at M=1 (fused norm+quant, then the dual GEMM on its
+    output): a CUDA graph of 8 steps on 8 cold rows, cycling over 4 copies of
+    the weights (176 MB, more than L2), with launch overlap on and off."""
+    stream = torch.cuda.current_stream()
+    wa, swa = dsnq.quantize_weight_block128(inputs.weight(N_ATTN, KQ, seed=0, salt=1).to(dev))
+    wi, swi = dsnq.quantize_weight_block128(inputs.weight(N_IDX, KQ, seed=0, salt=2).to(dev))
+    copies = [(wa, swa, wi, swi)] + [(wa.clone(), swa.clone(), wi.clone(), swi.clone()) for _ in range(3)]
+    oa = torch.empty(1, N_ATTN, dtype=torch.bfloat16, device=dev)
+    oi = torch.empty(1, N_IDX, dtype=torch.bfloat16, device=dev)
+
+    def step(r, c):
+        dsnq.fused_dual_rmsnorm_group_quant(buf[r:r + 1, :KQ], buf[r:r + 1, KQ:KQ + KKV], gq, gkv, eps,
+                                            q_out=qo, q_scale=so, kv_out=ko)
+        dsnq.block_scaled_fp8_gemm_dual(qo, so, c[0], c[1], c[2], c[3], out1=oa, out2=oi)
+
+    steps = [(lambda r=r: step(r, copies[r % 4])) for r in range(8)]
+    res = {}
+    for overlap in (True, False):
+        dsnq.set_launch_overlap(overlap)
+        res["overlap" if overlap else "no_overlap"] = round(timed_graph_calls(torch, stream, steps, flush), 3)
+    dsnq.set_launch_overlap(True)
+    res["note"] = ("us per step: fused norm+quant then the dual GEMM (44 MB of weights from HBM), CUDA graph of 8 "
+                   "steps on 8 cold rows over 4 weight copies; overlap = programmatic dependent launch (default)")
+    return res
 
 
 def gemm_sweep(torch, dsnq, inputs, dev, flush, hbm_gbs, args):

@@ -31,7 +31,8 @@ __all__ = [
     "ROW_MAJOR", "COL_MAJOR", "DsnqError",
     "fused_dual_rmsnorm_group_quant", "rmsnorm_group_quant", "dual_rmsnorm_bf16", "group_quant_bf16",
     "quantize_weight_block128", "block_scaled_fp8_gemm", "block_scaled_fp8_gemm_dual",
-    "quant_output_sizes", "debug_status", "debug_set", "scale_layout_of", "scale_ld_for", "empty_scales",
+    "quant_output_sizes", "debug_status", "debug_set", "set_launch_overlap", "scale_layout_of", "scale_ld_for",
+    "empty_scales",
 ]
 
 
@@ -226,3 +227,10 @@ def debug_status(stream=None) -> int:
 
 def debug_set(inject_flags: int = 0, wait_timeout_ns: int = 0) -> None:
     lib().dsnq_debug_set(inject_flags, wait_timeout_ns)
+
+
+def set_launch_overlap(enable: bool = True) -> None:
+    """Programmatic dependent launch for every later call (on by default):
+    a kernel may be scheduled while the previous kernel of its stream runs,
+    and waits in hardware for that kernel's writes before reading inputs."""
+    lib().dsnq_set_launch_overlap(1 if enable else 0)

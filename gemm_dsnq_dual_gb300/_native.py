@@ -43,6 +43,7 @@ SIGNATURES = {
               i64, vp, i64, vp, i64, vp, i64, vp]),
     "dsnq_debug_status": (i32, [vp]),
     "dsnq_debug_set": (None, [u32, u64]),
+    "dsnq_set_launch_overlap": (None, [i32]),
 }
 
 _lib = None

@@ -3,6 +3,8 @@
 // (vLLM PR #53540 prhub summary, _fused_mla_dual_rms_norm_group_quant_fake:
 // q_out [M, Nq] fp8 and q_scale [M, Nq / group_size] fp32).
 
+#include <atomic>
+
 #include "dsnq_internal.h"
 
 extern "C" const char* dsnq_status_string(dsnq_status status) {
@@ -18,6 +20,16 @@ extern "C" const char* dsnq_status_string(dsnq_status status) {
 }
 
 extern "C" int32_t dsnq_version(void) { return 100; }  // 0.1.0
+
+namespace {
+std::atomic<int> g_launch_overlap{1};
+}
+
+bool dsnq::launch_overlap_enabled() { return g_launch_overlap.load(std::memory_order_relaxed) != 0; }
+
+extern "C" void dsnq_set_launch_overlap(int32_t enable) {
+    g_launch_overlap.store(enable ? 1 : 0, std::memory_order_relaxed);
+}
 
 extern "C" dsnq_status dsnq_quant_output_sizes(int64_t M, int64_t Kq, int32_t group, dsnq_scale_layout layout,
                                                int64_t* n_scale_elems, int64_t* default_ld_scale) {

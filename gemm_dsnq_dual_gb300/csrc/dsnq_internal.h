@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cstdint>
+#include <utility>
 #include <cuda_runtime.h>
 
 #include "dsnq.h"
@@ -19,12 +20,55 @@ inline dsnq_status launch_status() {
     return e == cudaSuccess ? DSNQ_OK : DSNQ_ERR_CUDA;
 }
 
+// Status of a launch made with cudaLaunchKernelEx (its own return value and
+// the runtime's last-error slot, which is cleared).
+inline dsnq_status launch_result(cudaError_t e) {
+    const cudaError_t last = cudaGetLastError();
+    return (e == cudaSuccess && last == cudaSuccess) ? DSNQ_OK : DSNQ_ERR_CUDA;
+}
+
 inline int device_sm_count() {
     int dev = 0, n = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
     return n;
 }
+
+// Programmatic dependent launch.  When enabled (the default; see
+// dsnq_set_launch_overlap) every kernel is launched with programmatic stream
+// serialization: it may be scheduled while the previous kernel of the stream
+// still runs, sets up what depends on no input (barriers, tensor memory,
+// descriptor prefetch), then waits in hardware (griddepcontrol.wait) until
+// the previous kernel has completed and its writes are visible, before any
+// thread reads global memory.
+bool launch_overlap_enabled();
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                                 Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = launch_overlap_enabled() ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
+#ifdef __CUDACC__
+// Wait until the kernels this grid depends on have completed and their
+// memory operations are visible (returns at once for a plain launch).
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Allow the next kernel of the stream to be scheduled; it still waits for
+// this grid's completion before reading anything.
+__device__ __forceinline__ void allow_dependent_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+#endif
 
 // Validated scale-buffer geometry: returns the effective ld or -1.
 inline int64_t scale_ld(dsnq_scale_layout layout, int64_t M, int64_t G, int64_t ld) {

@@ -509,6 +509,10 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
     const uint64_t tmo = p.timeout_ns;
+    // Everything above reads no argument buffer; from here on every role
+    // reads inputs (or writes outputs that an earlier kernel may still read).
+    grid_dependency_wait();
+    allow_dependent_launch();
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer (2*STAGES lanes)
@@ -1017,6 +1021,8 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
     const uint64_t tmo = p.timeout_ns;
+    grid_dependency_wait();      // as in block_scaled_gemm_kernel
+    allow_dependent_launch();
 
     // Warp-group 0 (the role warps) hands registers to the promotion warps.
     if (warp < 4) {
@@ -1453,8 +1459,7 @@ dsnq_status launch(gemm::Params& prm, const CUtensorMap& ma, const CUtensorMap& 
     // walking the tile space with a stride of the grid size.
     const int sms = device_sm_count();
     const int grid = prm.total_tiles < sms ? prm.total_tiles : (sms > 0 ? sms : prm.total_tiles);
-    kern<<<grid, C::kThreads, smem, stream>>>(ma, mw0, mw1, mo0, mo1, prm);
-    return launch_status();
+    return launch_result(launch_kernel(kern, dim3(grid), dim3(C::kThreads), smem, stream, ma, mw0, mw1, mo0, mo1, prm));
 }
 
 // CTA-pair kernel: as many 2-CTA clusters as fit at once, each walking the
@@ -1466,11 +1471,13 @@ dsnq_status launch_pair(gemm::Params& prm, const CUtensorMap& ma, const CUtensor
     auto kern = gemm::pair_gemm_kernel;
     if (!set_smem_attr(reinterpret_cast<const void*>(kern), smem)) return DSNQ_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.blockDim = dim3(gemm::pair::kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
@@ -1489,11 +1496,8 @@ dsnq_status launch_pair(gemm::Params& prm, const CUtensorMap& ma, const CUtensor
     if (clusters <= 0) return DSNQ_ERR_UNSUPPORTED;
     const int n = prm.total_super < clusters ? prm.total_super : clusters;
     cfg.gridDim = dim3(2 * n, 1, 1);
-    if (cudaLaunchKernelEx(&cfg, kern, ma, mw0, mw1, mo0, mo1, prm) != cudaSuccess) {
-        cudaGetLastError();
-        return DSNQ_ERR_CUDA;
-    }
-    return DSNQ_OK;
+    cfg.numAttrs = launch_overlap_enabled() ? 2 : 1;
+    return launch_result(cudaLaunchKernelEx(&cfg, kern, ma, mw0, mw1, mo0, mo1, prm));
 }
 
 dsnq_status run_gemm(int64_t M, int64_t K, const void* a, int64_t lda, const float* as,

@@ -157,6 +157,8 @@ __device__ __forceinline__ float half_warp_max(float v) {
 template <int MODE, int PASSES>
 __global__ void __launch_bounds__(kThreads, min_blocks_per_sm(PASSES))
 row_norm_quant_kernel(const RowArgs a) {
+    grid_dependency_wait();      // inputs are read only once the previous kernel's writes are visible
+    allow_dependent_launch();
     const int t = threadIdx.x;
     const int lane = t & 31, warp = t >> 5;
 
@@ -279,6 +281,8 @@ constexpr int kRowCtasPerSM = 4;    // register budget: up to 128 per thread
 template <int MODE, int CPT>
 __global__ void __launch_bounds__(kRowWarps * 32, kRowCtasPerSM)
 warp_row_kernel(const RowArgs a) {
+    grid_dependency_wait();      // inputs are read only once the previous kernel's writes are visible
+    allow_dependent_launch();
     extern __shared__ float gamma_s[];          // [Kq + Kkv] fp32
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -451,6 +455,8 @@ constexpr int kFusedCtasPerSM = 4;  // register budget: 128 per thread
 template <int QS, int KS>
 __global__ void __launch_bounds__(kRowWarps * 32, kFusedCtasPerSM)
 warp_row_fused_kernel(const RowArgs a) {
+    grid_dependency_wait();      // inputs are read only once the previous kernel's writes are visible
+    allow_dependent_launch();
     constexpr int CPT = QS + KS;
     extern __shared__ float gamma_s[];          // [(QS + KS) * 256] fp32: gamma_q then gamma_kv
     const int lane = threadIdx.x & 31;
@@ -591,8 +597,8 @@ static dsnq_status launch_rows(RowArgs a, int64_t M, cudaStream_t s) {
         const int64_t rows_cap = sms > 0 ? static_cast<int64_t>(sms) * kFusedCtasPerSM : (M + kRowWarps - 1) / kRowWarps;
         const int64_t need = (M + kRowWarps - 1) / kRowWarps;
         dim3 grid(static_cast<unsigned>(need < rows_cap ? need : rows_cap)), block(kRowWarps * 32);
-        warp_row_fused_kernel<6, 2><<<grid, block, static_cast<size_t>(chunks) * kChunk * sizeof(float), s>>>(a);
-        return launch_status();
+        return launch_result(launch_kernel(warp_row_fused_kernel<6, 2>, grid, block,
+                                           static_cast<size_t>(chunks) * kChunk * sizeof(float), s, a));
     }
     if (chunks <= 8 * 32 && M >= warp_row_min) {
         // Warp per row.  Enough CTAs to fill every SM at the register-limited occupancy.
@@ -601,30 +607,32 @@ static dsnq_status launch_rows(RowArgs a, int64_t M, cudaStream_t s) {
         const int64_t need = (M + kRowWarps - 1) / kRowWarps;
         dim3 grid(static_cast<unsigned>(need < rows_cap ? need : rows_cap)), block(kRowWarps * 32);
         const size_t smem = MODE == kQuantOnly ? 0 : static_cast<size_t>(chunks) * kChunk * sizeof(float);
+        cudaError_t e;
         switch (cpt) {
-            case 1: warp_row_kernel<MODE, 1><<<grid, block, smem, s>>>(a); break;
-            case 2: warp_row_kernel<MODE, 2><<<grid, block, smem, s>>>(a); break;
-            case 3: warp_row_kernel<MODE, 3><<<grid, block, smem, s>>>(a); break;
-            case 4: warp_row_kernel<MODE, 4><<<grid, block, smem, s>>>(a); break;
-            case 5: warp_row_kernel<MODE, 5><<<grid, block, smem, s>>>(a); break;
-            case 6: warp_row_kernel<MODE, 6><<<grid, block, smem, s>>>(a); break;
-            case 7: warp_row_kernel<MODE, 7><<<grid, block, smem, s>>>(a); break;
-            default: warp_row_kernel<MODE, 8><<<grid, block, smem, s>>>(a); break;
+            case 1: e = launch_kernel(warp_row_kernel<MODE, 1>, grid, block, smem, s, a); break;
+            case 2: e = launch_kernel(warp_row_kernel<MODE, 2>, grid, block, smem, s, a); break;
+            case 3: e = launch_kernel(warp_row_kernel<MODE, 3>, grid, block, smem, s, a); break;
+            case 4: e = launch_kernel(warp_row_kernel<MODE, 4>, grid, block, smem, s, a); break;
+            case 5: e = launch_kernel(warp_row_kernel<MODE, 5>, grid, block, smem, s, a); break;
+            case 6: e = launch_kernel(warp_row_kernel<MODE, 6>, grid, block, smem, s, a); break;
+            case 7: e = launch_kernel(warp_row_kernel<MODE, 7>, grid, block, smem, s, a); break;
+            default: e = launch_kernel(warp_row_kernel<MODE, 8>, grid, block, smem, s, a); break;
         }
-        return launch_status();
+        return launch_result(e);
     }
     // Wider rows: one warp-group per row.  Enough CTAs to fill every SM at the
     // register-limited occupancy; each walks its rows with a grid stride.
     const int64_t cap = sms > 0 ? static_cast<int64_t>(sms) * min_blocks_per_sm(passes) : M;
     dim3 grid(static_cast<unsigned>(M < cap ? M : cap)), block(kThreads);
+    cudaError_t e;
     switch (passes) {
-        case 1: row_norm_quant_kernel<MODE, 1><<<grid, block, 0, s>>>(a); break;
-        case 2: row_norm_quant_kernel<MODE, 2><<<grid, block, 0, s>>>(a); break;
-        case 3: row_norm_quant_kernel<MODE, 3><<<grid, block, 0, s>>>(a); break;
-        case 4: row_norm_quant_kernel<MODE, 4><<<grid, block, 0, s>>>(a); break;
+        case 1: e = launch_kernel(row_norm_quant_kernel<MODE, 1>, grid, block, 0, s, a); break;
+        case 2: e = launch_kernel(row_norm_quant_kernel<MODE, 2>, grid, block, 0, s, a); break;
+        case 3: e = launch_kernel(row_norm_quant_kernel<MODE, 3>, grid, block, 0, s, a); break;
+        case 4: e = launch_kernel(row_norm_quant_kernel<MODE, 4>, grid, block, 0, s, a); break;
         default: return DSNQ_ERR_UNSUPPORTED;
     }
-    return launch_status();
+    return launch_result(e);
 }
 
 // ---------------------------------------------------------------------------
@@ -635,6 +643,8 @@ __global__ void __launch_bounds__(256)
 weight_block_quant_kernel(int64_t N, int64_t K, const float* __restrict__ w, int64_t ldw,
                           uint8_t* __restrict__ out, int64_t ldo,
                           float* __restrict__ sw, int64_t ldsw) {
+    grid_dependency_wait();      // inputs are read only once the previous kernel's writes are visible
+    allow_dependent_launch();
     const int64_t nb = blockIdx.y, kb = blockIdx.x;
     const int t = threadIdx.x;
     const int64_t row = nb * 128 + t / 2;
@@ -843,7 +853,7 @@ extern "C" dsnq_status dsnq_quantize_weight_block128(
     const int64_t nb = (N + 127) / 128;
     if (nb > 65535) return DSNQ_ERR_UNSUPPORTED;
     dim3 grid(static_cast<unsigned>(K / 128), static_cast<unsigned>(nb));
-    weight_block_quant_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
-        N, K, w, ldw, static_cast<uint8_t*>(w_fp8), ldw_out, w_scale, ld_wscale);
-    return launch_status();
+    return launch_result(launch_kernel(weight_block_quant_kernel, grid, dim3(256), 0,
+                                       static_cast<cudaStream_t>(stream), N, K, w, ldw,
+                                       static_cast<uint8_t*>(w_fp8), ldw_out, w_scale, ld_wscale));
 }

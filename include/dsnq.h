@@ -264,6 +264,20 @@ DSNQ_API dsnq_status dsnq_block_scaled_fp8_gemm_dual(
 DSNQ_API dsnq_status dsnq_debug_status(void* stream);
 
 /*
+ * Launch overlap (programmatic dependent launch), on by default; affects
+ * later launches of every entry point on all devices of this process.
+ * When on, each kernel is launched so that it may be scheduled while the
+ * previous kernel of its stream is still running: it prepares what reads no
+ * input (barriers, tensor memory, descriptors) and then waits in hardware
+ * until that kernel has completed and its writes are visible, before reading
+ * any argument buffer.  Results are identical either way; only the gap
+ * between dependent launches (a decode step's norm+quant and GEMM, say)
+ * shrinks.  enable = 0 restores plain stream ordering.  No counterpart in the
+ * published method: a launch property of this implementation.
+ */
+DSNQ_API void dsnq_set_launch_overlap(int32_t enable);
+
+/*
  * Test hooks for the bounded waits (affect later launches on all devices of
  * this process).  wait_timeout_ns bounds every device wait (0 restores the
  * default of 2 s).  inject_flags bit 0 makes the GEMM's producer skip the
