@@ -398,8 +398,24 @@ def decode_step(torch, dsnq, inputs, dev, flush, buf, gq, gkv, eps, qo, so, ko):
         dsnq.set_launch_overlap(overlap)
         res["overlap" if overlap else "no_overlap"] = round(timed_graph_calls(torch, stream, steps, flush), 3)
     dsnq.set_launch_overlap(True)
+
+    # bf16 activations without a pre-quantized pair: quantized inside the GEMM
+    # (one launch) against the quant kernel followed by the GEMM.
+    xa = inputs.activations_bf16(8, KQ, seed=9).to(dev)
+    so_col = dsnq.empty_scales(1, KQ // 128, "col", dev)
+    in_gemm = [(lambda r=r: dsnq.block_scaled_fp8_gemm_dual_bf16a(xa[r:r + 1], *copies[r % 4], out1=oa, out2=oi))
+               for r in range(8)]
+
+    def two_launches(r):
+        dsnq.group_quant_bf16(xa[r:r + 1], scale_layout="col", x_out=qo, x_scale=so_col)
+        dsnq.block_scaled_fp8_gemm_dual(qo, so_col, *copies[r % 4], out1=oa, out2=oi)
+
+    res["bf16_in_gemm_quant"] = round(timed_graph_calls(torch, stream, in_gemm, flush), 3)
+    res["bf16_quant_then_gemm"] = round(timed_graph_calls(torch, stream, [(lambda r=r: two_launches(r))
+                                                                          for r in range(8)], flush), 3)
     res["note"] = ("us per step: fused norm+quant then the dual GEMM (44 MB of weights from HBM), CUDA graph of 8 "
-                   "steps on 8 cold rows over 4 weight copies; overlap = programmatic dependent launch (default)")
+                   "steps on 8 cold rows over 4 weight copies; overlap = programmatic dependent launch (default); "
+                   "bf16_*: the dual GEMM on a bf16 row quantized inside the GEMM, or by the quant kernel first")
     return res
 
 

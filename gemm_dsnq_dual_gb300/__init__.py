@@ -31,6 +31,7 @@ __all__ = [
     "ROW_MAJOR", "COL_MAJOR", "DsnqError",
     "fused_dual_rmsnorm_group_quant", "rmsnorm_group_quant", "dual_rmsnorm_bf16", "group_quant_bf16",
     "quantize_weight_block128", "block_scaled_fp8_gemm", "block_scaled_fp8_gemm_dual",
+    "block_scaled_fp8_gemm_dual_bf16a", "fused_quant_fits",
     "quant_output_sizes", "debug_status", "debug_set", "set_launch_overlap", "scale_layout_of", "scale_ld_for",
     "empty_scales",
 ]
@@ -217,6 +218,40 @@ def block_scaled_fp8_gemm_dual(a_fp8, a_scale, w1_fp8, w1_scale, w2_fp8, w2_scal
         N2, w2_fp8.data_ptr(), _row_view_ok(w2_fp8, "w2_fp8"), w2_scale.data_ptr(),
         _row_view_ok(w2_scale, "w2_scale"), out2.data_ptr(), _row_view_ok(out2, "out2"),
         _stream(stream)), "dsnq_block_scaled_fp8_gemm_dual")
+    return out1, out2
+
+
+def fused_quant_fits(M: int, K: int) -> bool:
+    """True when block_scaled_fp8_gemm_dual_bf16a quantizes inside the GEMM
+    (one launch, no workspace)."""
+    return 0 < M <= 16 and K <= 2048 and M * ((K // 128 + 1) // 2) <= 40
+
+
+def block_scaled_fp8_gemm_dual_bf16a(a_bf16, w1_fp8, w1_scale, w2_fp8, w2_scale,
+                                     out1=None, out2=None, workspace=None, stream=None):
+    """The dual GEMM on bf16 activations, quantized per 1x128 on the fly.
+    `workspace` = (a_fp8 [M,K] uint8/e4m3, a_scale [M*K/128] fp32) is only
+    needed outside fused_quant_fits(M, K); it is allocated here if omitted."""
+    M, K = a_bf16.shape
+    N1, N2 = w1_fp8.shape[0], w2_fp8.shape[0]
+    dev = a_bf16.device
+    if out1 is None:
+        out1 = torch.empty(M, N1, dtype=torch.bfloat16, device=dev)
+    if out2 is None:
+        out2 = torch.empty(M, N2, dtype=torch.bfloat16, device=dev)
+    ws_a = ws_s = 0
+    if M > 0 and not fused_quant_fits(M, K):
+        if workspace is None:
+            workspace = (torch.empty(M, K, dtype=torch.uint8, device=dev),
+                         torch.empty(M * (K // GROUP), dtype=torch.float32, device=dev))
+        ws_a, ws_s = workspace[0].data_ptr(), workspace[1].data_ptr()
+    check(lib().dsnq_block_scaled_fp8_gemm_dual_bf16a(
+        M, K, a_bf16.data_ptr(), _row_view_ok(a_bf16, "a_bf16"),
+        N1, w1_fp8.data_ptr(), _row_view_ok(w1_fp8, "w1_fp8"), w1_scale.data_ptr(),
+        _row_view_ok(w1_scale, "w1_scale"), out1.data_ptr(), _row_view_ok(out1, "out1"),
+        N2, w2_fp8.data_ptr(), _row_view_ok(w2_fp8, "w2_fp8"), w2_scale.data_ptr(),
+        _row_view_ok(w2_scale, "w2_scale"), out2.data_ptr(), _row_view_ok(out2, "out2"),
+        ws_a, ws_s, _stream(stream)), "dsnq_block_scaled_fp8_gemm_dual_bf16a")
     return out1, out2
 
 

@@ -41,6 +41,11 @@ SIGNATURES = {
         i32, [i64, i64, vp, i64, vp, i32, i64,
               i64, vp, i64, vp, i64, vp, i64,
               i64, vp, i64, vp, i64, vp, i64, vp]),
+    "dsnq_block_scaled_fp8_gemm_dual_bf16a": (
+        i32, [i64, i64, vp, i64,
+              i64, vp, i64, vp, i64, vp, i64,
+              i64, vp, i64, vp, i64, vp, i64,
+              vp, vp, vp]),
     "dsnq_debug_status": (i32, [vp]),
     "dsnq_debug_set": (None, [u32, u64]),
     "dsnq_set_launch_overlap": (None, [i32]),

@@ -50,6 +50,7 @@
 #include <vector>
 
 #include "dsnq_internal.h"
+#include "group_quant.cuh"
 
 namespace dsnq {
 namespace gemm {
@@ -84,6 +85,8 @@ struct Params {
     Problem prob[2];
     uint64_t timeout_ns;
     uint32_t inject;
+    const __nv_bfloat16* a_bf16;   // activations quantized in the kernel (decode, bf16 input)
+    int64_t lda_bf16;
 };
 
 // ----------------------------------------------------------------- PTX glue
@@ -401,11 +404,16 @@ __host__ __device__ constexpr uint32_t idesc_e4m3(int bn) {
 //   STAGES    depth of the shared-memory ring (one 128-wide K block per stage)
 //   NBUF      TMEM partial-sum buffers (the MMA may run NBUF-1 K blocks ahead)
 //   EPI_WARPS promotion warps (a multiple of 4: one per TMEM lane quarter and slice)
-template <int BN, bool SWAP, int STAGES, int NBUF, int EPI_WARPS>
+//   AQ        (swap only) the activations arrive as bf16 and are quantized by
+//             the kernel into a resident shared-memory operand; the ring
+//             carries only the weights
+template <int BN, bool SWAP, int STAGES, int NBUF, int EPI_WARPS, bool AQ = false>
 struct Cfg {
     static constexpr int kPBytes = kPRows * kBK;       // 16 KB
-    static constexpr int kQBytes = BN * kBK;
+    static constexpr int kQBytes = AQ ? 0 : BN * kBK;
     static constexpr int kStageBytes = kPBytes + kQBytes;
+    static constexpr int kResBytes = BN * kBK;         // AQ: one K block of the resident operand
+    static_assert(!AQ || SWAP, "in-kernel activation quant is a decode (swap-AB) variant");
     static constexpr int kTmemNeed = NBUF * BN;
     static constexpr int kTmemCols = kTmemNeed <= 32 ? 32 : kTmemNeed <= 64 ? 64 : kTmemNeed <= 128 ? 128
                                      : kTmemNeed <= 256 ? 256 : 512;
@@ -427,6 +435,84 @@ struct Cfg {
     static_assert(SWAP || BN == kPRows, "non-swap tiles are 128 features wide");
 };
 
+// In-kernel per-1x128 quantization of the bf16 activations (decode) into
+// the resident operand: a K block's codes at a_res + kb*BN*128 in the layout
+// a 128-byte-swizzled TMA copy leaves (row r's 128 codes at r*128, 16-byte
+// chunk c at chunk c ^ (r & 7)); its scales to both scale slots ([kb][row],
+// the second one slot_stride floats on).  Rows past M are zero (codes and
+// scales, no arithmetic).  The live rows are cut into units of 256 columns
+// (one row slot: a group per half-warp) spread over the nw quantizer warps,
+// four units at a time per warp so that their latency chains (loads,
+// shuffles, the scale division) overlap.  The arithmetic is the norm+quant
+// kernels' (group_quant.cuh).
+template <int BN>
+__device__ __forceinline__ void quantize_activations(const Params& p, uint8_t* a_res, float* sa_slots,
+                                                     int slot_stride, int qw, int nw, int lane) {
+    constexpr int kU = 4;                       // units in flight per warp
+    const int KB = p.KB;
+    const int live = p.M < BN ? p.M : BN;
+    // Zero rows: bytes [live*128, BN*128) of every K block, and their scales.
+    const int zero_vec = (BN - live) * (kBK / 16);          // uint4 per K block
+    for (int e = qw * 32 + lane; e < KB * zero_vec; e += nw * 32) {
+        const int kb = e / zero_vec, v = e % zero_vec;
+        reinterpret_cast<uint4*>(a_res + kb * (BN * kBK) + live * kBK)[v] = make_uint4(0, 0, 0, 0);
+    }
+    for (int e = qw * 32 + lane; e < KB * (BN - live); e += nw * 32) {
+        const int kb = e / (BN - live), r = live + e % (BN - live);
+        sa_slots[kb * BN + r] = 0.f;
+        sa_slots[slot_stride + kb * BN + r] = 0.f;
+    }
+    const int slots = (KB + 1) / 2;
+    const int units = live * slots;
+    const int h = lane >> 4;                    // half-warp h of slot i holds group 2i + h
+    const int c16 = (lane & 15) >> 1;           // 16-byte chunk of the lane's 8 codes in the group's row
+    for (int u0 = qw; u0 < units; u0 += kU * nw) {
+        uint4 raw[kU];
+        int row[kU], kb[kU];
+        bool on[kU];
+#pragma unroll
+        for (int j = 0; j < kU; ++j) {
+            const int u = u0 + j * nw;
+            row[j] = u / slots;
+            const int slot = u - row[j] * slots;
+            kb[j] = 2 * slot + h;
+            on[j] = u < units && kb[j] < KB;    // odd KB: the last slot's second half is past the row
+            raw[j] = make_uint4(0, 0, 0, 0);
+            if (on[j])
+                raw[j] = __ldg(reinterpret_cast<const uint4*>(p.a_bf16 + static_cast<int64_t>(row[j]) * p.lda_bf16 +
+                                                               (slot * 32 + lane) * 8));
+        }
+        float2 x[kU][4];
+        float amax[kU];
+#pragma unroll
+        for (int j = 0; j < kU; ++j) {
+            unpack8(raw[j], x[j]);
+            amax[j] = fmaxf(fmaxf(fmaxf(fabsf(x[j][0].x), fabsf(x[j][0].y)), fmaxf(fabsf(x[j][1].x), fabsf(x[j][1].y))),
+                            fmaxf(fmaxf(fabsf(x[j][2].x), fabsf(x[j][2].y)), fmaxf(fabsf(x[j][3].x), fabsf(x[j][3].y))));
+        }
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) {
+#pragma unroll
+            for (int j = 0; j < kU; ++j) amax[j] = fmaxf(amax[j], __shfl_xor_sync(0xffffffffu, amax[j], o));
+        }
+#pragma unroll
+        for (int j = 0; j < kU; ++j) {
+            if (!on[j]) continue;
+            const GroupQuant gq = make_group_quant(amax[j]);
+            bool ok;
+            uint2 codes = quant8_bracket(x[j], gq, ok);
+            if (!ok) codes = quant8_divide(x[j], gq.scale);
+            const int r = row[j];
+            *reinterpret_cast<uint2*>(a_res + kb[j] * (BN * kBK) + r * kBK + ((c16 ^ (r & 7)) << 4) + (lane & 1) * 8) =
+                codes;
+            if ((lane & 15) == 0) {
+                sa_slots[kb[j] * BN + r] = gq.scale;
+                sa_slots[slot_stride + kb[j] * BN + r] = gq.scale;
+            }
+        }
+    }
+}
+
 // Tile t of the concatenated tile space -> (problem, first activation row, first feature).
 // Activation tiles vary fastest, so CTAs running together share weight tiles in L2.
 template <int BN, bool SWAP>
@@ -438,20 +524,21 @@ __device__ __forceinline__ void tile_coords(const Params& p, int t, int& pi, int
     n0 = SWAP ? tn * kPRows : tn * BN;
 }
 
-template <int BN, bool SWAP, int STAGES, int NBUF, int EPI_WARPS>
-__global__ void __launch_bounds__(Cfg<BN, SWAP, STAGES, NBUF, EPI_WARPS>::kThreads, 1)
+template <int BN, bool SWAP, int STAGES, int NBUF, int EPI_WARPS, bool AQ = false>
+__global__ void __launch_bounds__(Cfg<BN, SWAP, STAGES, NBUF, EPI_WARPS, AQ>::kThreads, 1)
 block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                          const __grid_constant__ CUtensorMap map_w0,
                          const __grid_constant__ CUtensorMap map_w1,
                          const __grid_constant__ CUtensorMap map_o0,
                          const __grid_constant__ CUtensorMap map_o1,
                          const Params p) {
-    using C = Cfg<BN, SWAP, STAGES, NBUF, EPI_WARPS>;
+    using C = Cfg<BN, SWAP, STAGES, NBUF, EPI_WARPS, AQ>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 1024-byte alignment for the 128-byte-swizzled tiles.
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* tiles = smem;
-    uint8_t* out_stage = smem + STAGES * C::kStageBytes;      // [EPI_WARPS][kStageOutBytes]
+    uint8_t* a_res = smem + STAGES * C::kStageBytes;          // AQ: [KB][BN rows][128] e4m3, resident
+    uint8_t* out_stage = a_res + (AQ ? p.KB * C::kResBytes : 0);   // [EPI_WARPS][kStageOutBytes]
     uint64_t* bars = reinterpret_cast<uint64_t*>(out_stage + EPI_WARPS * C::kStageOutBytes);
     uint64_t* full = bars;                    // [STAGES] TMA -> MMA
     uint64_t* empty = bars + STAGES;          // [STAGES] MMA -> TMA
@@ -460,7 +547,8 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
     uint64_t* sfull = tempty + NBUF;          // [2]      scale loader -> promotion
     uint64_t* sempty = sfull + 2;             // [2]      promotion -> scale loader
     uint64_t* drain = sempty + 2;             // [1]      abort drain of MMAs
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+    uint64_t* aready = drain + 1;             // [1]      AQ: quantizer warps -> MMA, promotion
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(aready + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
     // Scale slots (16-byte aligned), K blocks padded to KBP = a multiple of 4:
     // [2][KBP][kScaleCols] raw activation scales (per P row for non-swap, per
@@ -488,9 +576,10 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
             mbar_init(smem_u32(&sempty[i]), EPI_WARPS);
         }
         mbar_init(smem_u32(drain), 1);
+        mbar_init(smem_u32(aready), C::kThreads / 32 - 2);   // every warp but the producer and the MMA warp
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        tma_prefetch_desc(&map_a);
+        if (!AQ) tma_prefetch_desc(&map_a);
         tma_prefetch_desc(&map_w0);
         tma_prefetch_desc(&map_w1);
         if (!SWAP) {
@@ -514,6 +603,15 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
     grid_dependency_wait();
     allow_dependent_launch();
 
+    if (AQ && warp >= 2) {
+        // Quantize the activations once for all of this CTA's tiles, while the
+        // producer already streams weights into the ring.
+        quantize_activations<BN>(p, a_res, sa_slots, KBP * C::kScaleCols, warp - 2, C::kThreads / 32 - 2, lane);
+        fence_proxy_async_smem();             // generic-proxy writes -> visible to the tensor core
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(aready));
+    }
+
     if (warp == 0) {
         // ------------------------------------------------ TMA producer (2*STAGES lanes)
         // A thread's bulk copies complete one after another (about one per L2
@@ -521,7 +619,7 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
         // lanes, each running its own loop: lane 2s loads the P tile of the K
         // blocks that use stage s (and arms the stage's barrier), lane 2s+1
         // their Q tile.  The lanes never wait for one another.
-        if (lane < 2 * STAGES) {
+        if (lane < 2 * STAGES && !(AQ && (lane & 1))) {   // AQ: no activation copies
             const int ntl = blockIdx.x < total ? (total - 1 - blockIdx.x) / gridDim.x + 1 : 0;
             const uint32_t ng = static_cast<uint32_t>(ntl) * KB;   // K blocks of this CTA
             const int s = lane >> 1;
@@ -573,9 +671,11 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
             // Descriptors of stage 0; stage s and K slice k only move the start
             // address field (16-byte units), which stays below 2^14 for 227 KB.
             const uint64_t dp0 = smem_desc_k_sw128(smem_u32(tiles));
-            const uint64_t dq0 = smem_desc_k_sw128(smem_u32(tiles + C::kPBytes));
+            const uint64_t dq0 = smem_desc_k_sw128(smem_u32(AQ ? a_res : tiles + C::kPBytes));
             uint32_t g = 0;
-            bool ok = true, any = false;
+            // Spinning waits (as on the MMA <-> promotion ring): a sleeping
+            // wait here would add its wake-up latency to every launch.
+            bool ok = !AQ || wait_bounded<true>(smem_u32(aready), 0, abort_flag, tmo), any = false;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
                 for (int kb = 0; kb < KB; ++kb, ++g) {
                     const int s = g % STAGES;
@@ -587,11 +687,13 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                     }
                     tc_fence_after();
                     const uint64_t so = static_cast<uint64_t>((s * C::kStageBytes) >> 4);
+                    // Q: the stage's slot, or the resident operand's K block.
+                    const uint64_t qo = AQ ? static_cast<uint64_t>((kb * C::kResBytes) >> 4) : so;
                     const uint32_t d = tmem_base + static_cast<uint32_t>(b * BN);
 #pragma unroll
                     for (int k = 0; k < kBK / kUmmaK; ++k) {
-                        const uint64_t ko = so + static_cast<uint64_t>((k * kUmmaK) >> 4);
-                        tc_mma_f8(d, dp0 + ko, dq0 + ko, idesc, k > 0 ? 1u : 0u);
+                        const uint64_t ko = static_cast<uint64_t>((k * kUmmaK) >> 4);
+                        tc_mma_f8(d, dp0 + so + ko, dq0 + qo + ko, idesc, k > 0 ? 1u : 0u);
                     }
                     tc_commit(smem_u32(&empty[s]));    // stage free once these MMAs have read it
                     tc_commit(smem_u32(&tfull[b]));    // partial sum ready
@@ -621,7 +723,9 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
             const float* sw = pr.w_scale + static_cast<int64_t>(n0 / kPRows) * pr.ld_ws;
             float* sa_dst = sa_slots + slot * KBP * C::kScaleCols;   // [kb][kScaleCols]
             const int rows = p.M - m0 < C::kScaleCols ? p.M - m0 : C::kScaleCols;
-            if (p.vec_scales && rows == C::kScaleCols) {
+            if (AQ) {
+                // Activation scales were written by the quantizer warps.
+            } else if (p.vec_scales && rows == C::kScaleCols) {
                 // Column-major scales with 16-byte aligned columns: each K block's
                 // run of kScaleCols scales is contiguous, 16 bytes per lane per copy
                 // (few, large copies: a thread's copies complete one at a time).
@@ -660,6 +764,7 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
         const int col0 = slice * C::kCols;
         uint32_t g = 0;
         bool ok = true;
+        if (AQ) ok = __all_sync(0xffffffffu, wait_bounded<true>(smem_u32(aready), 0, abort_flag, tmo));   // scales written
         int i = 0;
         for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++i) {
             int pi, m0, n0;
@@ -811,12 +916,12 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
     }
 }
 
-template <int BN, bool SWAP, int STAGES, int NBUF, int EPI_WARPS>
+template <int BN, bool SWAP, int STAGES, int NBUF, int EPI_WARPS, bool AQ = false>
 constexpr size_t smem_bytes(int KB) {
-    using C = Cfg<BN, SWAP, STAGES, NBUF, EPI_WARPS>;
+    using C = Cfg<BN, SWAP, STAGES, NBUF, EPI_WARPS, AQ>;
     const int KBP = (KB + 3) & ~3;
-    return 1024 /* alignment slack */ + STAGES * C::kStageBytes + EPI_WARPS * C::kStageOutBytes +
-           (2 * STAGES + 2 * NBUF + 5) * 8 + 16 + 16 +
+    return 1024 /* alignment slack */ + STAGES * C::kStageBytes + (AQ ? static_cast<size_t>(KB) * C::kResBytes : 0) +
+           EPI_WARPS * C::kStageOutBytes + (2 * STAGES + 2 * NBUF + 6) * 8 + 16 + 16 +
            static_cast<size_t>(2 * KBP * C::kScaleCols + 2 * KBP) * 4;
 }
 
@@ -1435,6 +1540,16 @@ struct Consumer {
     int64_t ldo;
 };
 
+// Every CTA quantizes all M rows itself, so the in-GEMM quantization pays
+// only while each of its ten quantizer warps has one batch of four 256-column
+// units (measured on GB300 at K=1536: M=1 12.6 us vs 14.1 us for the quant
+// kernel then the GEMM; M=16 17.3 vs 14.9 us).  At most 16 rows (MMA N=16),
+// K <= 2048.
+bool bf16a_in_gemm(int64_t M, int64_t K) {
+    const int64_t slots = (K / 128 + 1) / 2;
+    return M >= 1 && M <= 16 && K <= 2048 && M * slots <= 40;
+}
+
 dsnq_status check_consumer(const Consumer& c, int64_t K) {
     if (c.N < 0) return DSNQ_ERR_INVALID_ARG;
     if (c.N == 0) return DSNQ_OK;
@@ -1447,12 +1562,12 @@ dsnq_status check_consumer(const Consumer& c, int64_t K) {
     return DSNQ_OK;
 }
 
-template <int BN, bool SWAP, int STAGES, int NBUF, int EPI_WARPS>
+template <int BN, bool SWAP, int STAGES, int NBUF, int EPI_WARPS, bool AQ = false>
 dsnq_status launch(gemm::Params& prm, const CUtensorMap& ma, const CUtensorMap& mw0, const CUtensorMap& mw1,
                    const CUtensorMap& mo0, const CUtensorMap& mo1, cudaStream_t stream) {
-    using C = gemm::Cfg<BN, SWAP, STAGES, NBUF, EPI_WARPS>;
-    auto kern = gemm::block_scaled_gemm_kernel<BN, SWAP, STAGES, NBUF, EPI_WARPS>;
-    const size_t smem = gemm::smem_bytes<BN, SWAP, STAGES, NBUF, EPI_WARPS>(prm.KB);
+    using C = gemm::Cfg<BN, SWAP, STAGES, NBUF, EPI_WARPS, AQ>;
+    auto kern = gemm::block_scaled_gemm_kernel<BN, SWAP, STAGES, NBUF, EPI_WARPS, AQ>;
+    const size_t smem = gemm::smem_bytes<BN, SWAP, STAGES, NBUF, EPI_WARPS, AQ>(prm.KB);
     if (smem > 227 * 1024) return DSNQ_ERR_UNSUPPORTED;
     if (!set_smem_attr(reinterpret_cast<const void*>(kern), smem)) return DSNQ_ERR_CUDA;
     // Persistent: one CTA per SM (the shared-memory ring allows one), each
@@ -1500,20 +1615,30 @@ dsnq_status launch_pair(gemm::Params& prm, const CUtensorMap& ma, const CUtensor
     return launch_result(cudaLaunchKernelEx(&cfg, kern, ma, mw0, mw1, mo0, mo1, prm));
 }
 
+// a_bf16 != NULL selects the decode variant that quantizes bf16 activations
+// itself (see bf16a_in_gemm); a, as and the scale layout are then unused.
 dsnq_status run_gemm(int64_t M, int64_t K, const void* a, int64_t lda, const float* as,
                      dsnq_scale_layout layout, int64_t ld_as, const Consumer& c0, const Consumer& c1,
-                     void* stream) {
+                     void* stream, const void* a_bf16 = nullptr, int64_t lda_bf16 = 0) {
+    const bool aq = a_bf16 != nullptr;
     if (M < 0 || K <= 0 || c0.N < 0 || c1.N < 0) return DSNQ_ERR_INVALID_ARG;
-    if (layout != DSNQ_SCALE_ROW_MAJOR && layout != DSNQ_SCALE_COL_MAJOR) return DSNQ_ERR_INVALID_ARG;
+    if (!aq && layout != DSNQ_SCALE_ROW_MAJOR && layout != DSNQ_SCALE_COL_MAJOR) return DSNQ_ERR_INVALID_ARG;
     if (K % 128 != 0) return DSNQ_ERR_UNSUPPORTED;
     if (M > 0x7fffffffLL || K > 8192) return DSNQ_ERR_UNSUPPORTED;
+    if (aq && !bf16a_in_gemm(M, K)) return DSNQ_ERR_UNSUPPORTED;
     if (M == 0) return DSNQ_OK;          // empty activations may come with NULL pointers
-    if (!a || !as) return DSNQ_ERR_INVALID_ARG;
-    if (lda < K) return DSNQ_ERR_INVALID_ARG;
     const int64_t KB = K / 128;
-    const int64_t ld = scale_ld(layout, M, KB, ld_as);
-    if (ld < 0) return DSNQ_ERR_INVALID_ARG;
-    if (!aligned(a, 16) || lda % 16 || !aligned(as, 4)) return DSNQ_ERR_MISALIGNED;
+    int64_t ld = 0;
+    if (aq) {
+        if (lda_bf16 < K) return DSNQ_ERR_INVALID_ARG;
+        if (!aligned(a_bf16, 16) || lda_bf16 % 8) return DSNQ_ERR_MISALIGNED;
+    } else {
+        if (!a || !as) return DSNQ_ERR_INVALID_ARG;
+        if (lda < K) return DSNQ_ERR_INVALID_ARG;
+        ld = scale_ld(layout, M, KB, ld_as);
+        if (ld < 0) return DSNQ_ERR_INVALID_ARG;
+        if (!aligned(a, 16) || lda % 16 || !aligned(as, 4)) return DSNQ_ERR_MISALIGNED;
+    }
     dsnq_status st = check_consumer(c0, K);
     if (st != DSNQ_OK) return st;
     st = check_consumer(c1, K);
@@ -1538,12 +1663,14 @@ dsnq_status run_gemm(int64_t M, int64_t K, const void* a, int64_t lda, const flo
     prm.a_scale = as;
     if (layout == DSNQ_SCALE_ROW_MAJOR) { prm.as_rs = ld; prm.as_gs = 1; }
     else { prm.as_rs = 1; prm.as_gs = ld; }
-    prm.vec_scales = layout == DSNQ_SCALE_COL_MAJOR && ld % 4 == 0 && aligned(as, 16);
+    prm.vec_scales = !aq && layout == DSNQ_SCALE_COL_MAJOR && ld % 4 == 0 && aligned(as, 16);
+    prm.a_bf16 = static_cast<const __nv_bfloat16*>(a_bf16);
+    prm.lda_bf16 = lda_bf16;
     const int64_t rows_per_a_tile = swap ? bn : gemm::kPRows;
     prm.tiles_m = static_cast<int>((M + rows_per_a_tile - 1) / rows_per_a_tile);
 
     CUtensorMap ma, mw[2], mo[2];
-    if (!cached_map(&ma, a, M, K, lda, a_box)) return DSNQ_ERR_CUDA;
+    if (!aq && !cached_map(&ma, a, M, K, lda, a_box)) return DSNQ_ERR_CUDA;
     const Consumer* cs[2] = {&c0, &c1};
     int64_t total = 0, total_super = 0;
     int np = 0;
@@ -1576,6 +1703,7 @@ dsnq_status run_gemm(int64_t M, int64_t K, const void* a, int64_t lda, const flo
         mo[1] = mo[0];
     }
     if (swap) mo[0] = mo[1] = mw[0];   // unused by the decode variant
+    if (aq) ma = mw[0];                 // unused: the kernel quantizes the activations itself
     if (total > 0x7fffffffLL) return DSNQ_ERR_UNSUPPORTED;
     prm.total_tiles = static_cast<int>(total);
     prm.total_super = static_cast<int>(total_super);
@@ -1584,6 +1712,7 @@ dsnq_status run_gemm(int64_t M, int64_t K, const void* a, int64_t lda, const flo
     prm.inject = g_inject.load();
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (aq) return launch<16, true, 8, 32, 8, true>(prm, ma, mw[0], mw[1], mo[0], mo[1], s);
     if (paired) return launch_pair(prm, ma, mw[0], mw[1], mo[0], mo[1], s);
     switch (bn) {
         // Decode: the MMA per K block is tiny, so the MMA <-> promotion round
@@ -1621,6 +1750,33 @@ extern "C" dsnq_status dsnq_block_scaled_fp8_gemm_dual(
     Consumer c0{N1, w1_fp8, ldw1, w1_scale, ld_w1scale, out1_bf16, ldo1};
     Consumer c1{N2, w2_fp8, ldw2, w2_scale, ld_w2scale, out2_bf16, ldo2};
     return run_gemm(M, K, a_fp8, lda, a_scale, a_scale_layout, ld_ascale, c0, c1, stream);
+}
+
+extern "C" dsnq_status dsnq_block_scaled_fp8_gemm_dual_bf16a(
+    int64_t M, int64_t K, const void* a_bf16, int64_t lda, int64_t N1, const void* w1_fp8, int64_t ldw1,
+    const float* w1_scale, int64_t ld_w1scale, void* out1_bf16, int64_t ldo1, int64_t N2, const void* w2_fp8,
+    int64_t ldw2, const float* w2_scale, int64_t ld_w2scale, void* out2_bf16, int64_t ldo2, void* a_fp8_ws,
+    float* a_scale_ws, void* stream) {
+    Consumer c0{N1, w1_fp8, ldw1, w1_scale, ld_w1scale, out1_bf16, ldo1};
+    Consumer c1{N2, w2_fp8, ldw2, w2_scale, ld_w2scale, out2_bf16, ldo2};
+    if (M < 0 || K <= 0 || N1 < 0 || N2 < 0) return DSNQ_ERR_INVALID_ARG;
+    if (K % 128 != 0 || K > 4096) return DSNQ_ERR_UNSUPPORTED;
+    if (M == 0) return DSNQ_OK;
+    if (!a_bf16) return DSNQ_ERR_INVALID_ARG;
+    dsnq_status st = check_consumer(c0, K);
+    if (st != DSNQ_OK) return st;
+    st = check_consumer(c1, K);
+    if (st != DSNQ_OK) return st;
+    if (N1 == 0 && N2 == 0) return DSNQ_OK;
+    if (bf16a_in_gemm(M, K))   // a few decode rows: one launch, the kernel quantizes them itself
+        return run_gemm(M, K, nullptr, 0, nullptr, DSNQ_SCALE_ROW_MAJOR, 0, c0, c1, stream, a_bf16, lda);
+    // Otherwise quantize once into the caller's workspace, then the GEMM on
+    // the pre-quantized pair (inside the GEMM every CTA would redo it).
+    if (!a_fp8_ws || !a_scale_ws) return DSNQ_ERR_INVALID_ARG;
+    if (!aligned(a_fp8_ws, 16) || !aligned(a_scale_ws, 4)) return DSNQ_ERR_MISALIGNED;
+    st = dsnq_group_quant_bf16(M, K, a_bf16, lda, 128, a_fp8_ws, K, a_scale_ws, DSNQ_SCALE_COL_MAJOR, M, stream);
+    if (st != DSNQ_OK) return st;
+    return run_gemm(M, K, a_fp8_ws, K, a_scale_ws, DSNQ_SCALE_COL_MAJOR, M, c0, c1, stream);
 }
 
 extern "C" dsnq_status dsnq_debug_status(void* stream) {

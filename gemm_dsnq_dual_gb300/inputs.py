@@ -138,6 +138,18 @@ def weight(N: int, K: int = KQ, seed: int = 0, salt: int = 0, std: float = 0.02)
     return torch.randn(N, K, generator=g) * std
 
 
+def activations_bf16(M: int, K: int, seed: int, zero_rows=()) -> torch.Tensor:
+    """bf16 activations [M, K] N(0, 1) with 1% of the columns scaled by 30
+    (outlier channels), and the listed rows all zero."""
+    g = _gen(seed, 700 + M)
+    x = torch.randn(M, K, generator=g)
+    cols = torch.randperm(K, generator=g)[: max(1, K // 100)]
+    x[:, cols] *= 30.0
+    for r in zero_rows:
+        x[r] = 0.0
+    return x.to(torch.bfloat16)
+
+
 def random_codes_and_scales(M: int, K: int, seed: int):
     """Arbitrary finite E4M3FN codes [M, K] (uint8, NaN codes excluded) and
     positive fp32 scales [M, K/128] drawn directly, for GEMM tests that need

@@ -256,6 +256,38 @@ DSNQ_API dsnq_status dsnq_block_scaled_fp8_gemm_dual(
     void* stream);
 
 /*
+ * The dual GEMM for callers without a pre-quantized pair: bf16 activations
+ * are quantized per 1x128 group on the fly, then multiplied as in
+ * dsnq_block_scaled_fp8_gemm_dual (sglang PR #27289, aiter_w8a8_block_fp8_linear:
+ * when no input_scale is given, the input is quantized in the current step by
+ * the per-1x128 quant kernel before the block-scaled GEMM).  The quantization
+ * is that of dsnq_group_quant_bf16: per group of 128 values of a row,
+ * sa = fp32(amax / 448) and code = e4m3_rn_satfinite(fp32(a / sa)).
+ *   a_bf16, lda : bf16 [M, K], lda >= K, lda % 8 == 0, 16-byte aligned.
+ *   consumers   : as in dsnq_block_scaled_fp8_gemm_dual (N2 == 0: one consumer).
+ *   a_fp8_ws, a_scale_ws : caller-owned workspace for the quantized pair,
+ *                 M*K bytes (16-byte aligned) and M*(K/128) floats (4-byte
+ *                 aligned, written column-major).  Unused, and may be NULL,
+ *                 when M <= 16, K <= 2048 and M * ceil(K/256) <= 40 (M <= 6
+ *                 at K = 1536): there one launch quantizes the activations
+ *                 inside the GEMM, into shared memory.  Every CTA quantizes
+ *                 all M rows, so larger batches run the quant kernel into the
+ *                 workspace and then the GEMM (two launches).
+ * K must be a multiple of 128 and at most 4096.  DSNQ_ERR_INVALID_ARG when the
+ * workspace is needed and NULL.  The outputs must not overlap the inputs or
+ * the workspace.
+ */
+DSNQ_API dsnq_status dsnq_block_scaled_fp8_gemm_dual_bf16a(
+    int64_t M, int64_t K,
+    const void* a_bf16, int64_t lda,
+    int64_t N1, const void* w1_fp8, int64_t ldw1, const float* w1_scale, int64_t ld_w1scale,
+    void* out1_bf16, int64_t ldo1,
+    int64_t N2, const void* w2_fp8, int64_t ldw2, const float* w2_scale, int64_t ld_w2scale,
+    void* out2_bf16, int64_t ldo2,
+    void* a_fp8_ws, float* a_scale_ws,
+    void* stream);
+
+/*
  * Device status word.  Kernels with bounded waits (the GEMM's mbarrier
  * waits) record a timeout there instead of hanging.  This call synchronizes
  * `stream`, reads the word of the current device, clears it and returns

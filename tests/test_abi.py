@@ -139,6 +139,27 @@ def test_single_latent_argument_checks(lib):
     assert f(4, 1536, None, 1536, A, 1e-6, 128, A, 1536, A, 0, 0, None) == INVALID        # null x
 
 
+def test_bf16_activation_gemm_argument_checks(lib):
+    f = lib.dsnq_block_scaled_fp8_gemm_dual_bf16a
+
+    def call(M=4, K=1536, a=A, lda=1536, N1=512, ldo1=512, N2=256, ws=(None, None)):
+        return f(M, K, a, lda, N1, A, K, A, K // 128, A, ldo1, N2, A, K, A, K // 128, A, 256,
+                 ws[0], ws[1], None)
+
+    assert call(M=0) == OK
+    assert call(M=-1) == INVALID
+    assert call(K=1000, lda=1000) == UNSUPPORTED
+    assert call(K=8192, lda=8192) == UNSUPPORTED           # K > 4096
+    assert call(a=None) == INVALID
+    assert call(N1=520, ldo1=520) == UNSUPPORTED           # N % 16
+    assert call(N1=0, N2=0) == OK
+    assert call(M=100) == INVALID                          # workspace needed above 64 rows
+    assert call(M=100, ws=(A + 8, A)) == MISALIGNED
+    assert call(lda=1000) == INVALID                       # in-kernel quant path (M <= 64)
+    assert call(a=A + 8) == MISALIGNED
+    assert call(lda=1540) == MISALIGNED
+
+
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(_native, "_lib", None)
     monkeypatch.setattr(_native, "LIB_PATH", str(tmp_path / "libdsnq.so"))
