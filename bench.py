@@ -413,8 +413,13 @@ def decode_step(torch, dsnq, inputs, dev, flush, buf, gq, gkv, eps, qo, so, ko):
     res["bf16_in_gemm_quant"] = round(timed_graph_calls(torch, stream, in_gemm, flush), 3)
     res["bf16_quant_then_gemm"] = round(timed_graph_calls(torch, stream, [(lambda r=r: two_launches(r))
                                                                           for r in range(8)], flush), 3)
+    one = [(lambda r=r: dsnq.fused_norm_quant_gemm_dual(buf[r:r + 1, :KQ], buf[r:r + 1, KQ:KQ + KKV], gq, gkv, eps,
+                                                        *copies[r % 4], out1=oa, out2=oi, kv_out=ko))
+           for r in range(8)]
+    res["one_launch"] = round(timed_graph_calls(torch, stream, one, flush), 3)
     res["note"] = ("us per step: fused norm+quant then the dual GEMM (44 MB of weights from HBM), CUDA graph of 8 "
                    "steps on 8 cold rows over 4 weight copies; overlap = programmatic dependent launch (default); "
+                   "one_launch: the same step with the norm+quant inside the GEMM; "
                    "bf16_*: the dual GEMM on a bf16 row quantized inside the GEMM, or by the quant kernel first")
     return res
 

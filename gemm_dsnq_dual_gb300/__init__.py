@@ -31,7 +31,7 @@ __all__ = [
     "ROW_MAJOR", "COL_MAJOR", "DsnqError",
     "fused_dual_rmsnorm_group_quant", "rmsnorm_group_quant", "dual_rmsnorm_bf16", "group_quant_bf16",
     "quantize_weight_block128", "block_scaled_fp8_gemm", "block_scaled_fp8_gemm_dual",
-    "block_scaled_fp8_gemm_dual_bf16a", "fused_quant_fits",
+    "block_scaled_fp8_gemm_dual_bf16a", "fused_quant_fits", "fused_norm_quant_gemm_dual",
     "quant_output_sizes", "debug_status", "debug_set", "set_launch_overlap", "scale_layout_of", "scale_ld_for",
     "empty_scales",
 ]
@@ -253,6 +253,45 @@ def block_scaled_fp8_gemm_dual_bf16a(a_bf16, w1_fp8, w1_scale, w2_fp8, w2_scale,
         _row_view_ok(w2_scale, "w2_scale"), out2.data_ptr(), _row_view_ok(out2, "out2"),
         ws_a, ws_s, _stream(stream)), "dsnq_block_scaled_fp8_gemm_dual_bf16a")
     return out1, out2
+
+
+def fused_norm_quant_gemm_dual(q, kv, gamma_q, gamma_kv, eps, w1_fp8, w1_scale, w2_fp8, w2_scale,
+                               out1=None, out2=None, kv_out=None, q_fp8=None, q_scale=None, stream=None):
+    """RMSNorm + per-1x128 quant of the q latent (kv latent normalized to
+    bf16), then the dual GEMM, in one call.  Returns (out1, out2, kv_out,
+    q_fp8, q_scale); the last two are None when the rows were quantized
+    inside the GEMM and no buffers were passed."""
+    M, Kq = q.shape
+    Kkv = kv.shape[1]
+    N1, N2 = w1_fp8.shape[0], w2_fp8.shape[0]
+    dev = q.device
+    if out1 is None:
+        out1 = torch.empty(M, N1, dtype=torch.bfloat16, device=dev)
+    if out2 is None:
+        out2 = torch.empty(M, N2, dtype=torch.bfloat16, device=dev)
+    if kv_out is None:
+        kv_out = torch.empty(M, Kkv, dtype=torch.bfloat16, device=dev)
+    one_launch = fused_quant_fits(M, Kq) and Kkv <= 2048 and N1 + N2 > 0
+    if not one_launch and M > 0:
+        if q_fp8 is None:
+            q_fp8 = torch.empty(M, Kq, dtype=torch.float8_e4m3fn, device=dev)
+        if q_scale is None:
+            q_scale = empty_scales(M, Kq // GROUP, COL_MAJOR, dev)
+    for t, name in ((q_fp8, "q_fp8"), (q_scale, "q_scale")):
+        if t is not None and name == "q_fp8" and not t.is_contiguous():
+            raise ValueError("q_fp8 must be contiguous [M, Kq]")
+    if q_scale is not None and M > 1 and q_scale.stride() != (1, M):
+        raise ValueError("q_scale must be column-major [M, Kq/128] (strides (1, M))")
+    check(lib().dsnq_fused_norm_quant_gemm_dual(
+        M, Kq, Kkv, q.data_ptr(), _row_view_ok(q, "q"), kv.data_ptr(), _row_view_ok(kv, "kv"),
+        gamma_q.data_ptr(), gamma_kv.data_ptr(), float(eps), kv_out.data_ptr(), _row_view_ok(kv_out, "kv_out"),
+        N1, w1_fp8.data_ptr(), _row_view_ok(w1_fp8, "w1_fp8"), w1_scale.data_ptr(),
+        _row_view_ok(w1_scale, "w1_scale"), out1.data_ptr(), _row_view_ok(out1, "out1"),
+        N2, w2_fp8.data_ptr(), _row_view_ok(w2_fp8, "w2_fp8"), w2_scale.data_ptr(),
+        _row_view_ok(w2_scale, "w2_scale"), out2.data_ptr(), _row_view_ok(out2, "out2"),
+        0 if q_fp8 is None else q_fp8.data_ptr(), 0 if q_scale is None else q_scale.data_ptr(),
+        _stream(stream)), "dsnq_fused_norm_quant_gemm_dual")
+    return out1, out2, kv_out, q_fp8, q_scale
 
 
 def debug_status(stream=None) -> int:

@@ -41,6 +41,11 @@ SIGNATURES = {
         i32, [i64, i64, vp, i64, vp, i32, i64,
               i64, vp, i64, vp, i64, vp, i64,
               i64, vp, i64, vp, i64, vp, i64, vp]),
+    "dsnq_fused_norm_quant_gemm_dual": (
+        i32, [i64, i64, i64, vp, i64, vp, i64, vp, vp, f32, vp, i64,
+              i64, vp, i64, vp, i64, vp, i64,
+              i64, vp, i64, vp, i64, vp, i64,
+              vp, vp, vp]),
     "dsnq_block_scaled_fp8_gemm_dual_bf16a": (
         i32, [i64, i64, vp, i64,
               i64, vp, i64, vp, i64, vp, i64,

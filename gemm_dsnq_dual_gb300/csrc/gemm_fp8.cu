@@ -87,6 +87,18 @@ struct Params {
     uint32_t inject;
     const __nv_bfloat16* a_bf16;   // activations quantized in the kernel (decode, bf16 input)
     int64_t lda_bf16;
+    // In-kernel RMSNorm of those activations (AQ == 2) and its side outputs,
+    // written by CTA 0: kv_out, and optionally the codes and scales.
+    const __nv_bfloat16* gamma_q;
+    const __nv_bfloat16* kv;
+    const __nv_bfloat16* gamma_kv;
+    int64_t ldkv;
+    int kkv;
+    float kq_f, kkv_f, eps;
+    __nv_bfloat16* kv_out;
+    int64_t ldkv_out;
+    uint8_t* q_out;                // [M, K] e4m3, row stride K (NULL: not written)
+    float* qs_out;                 // [M, K/128] column-major, ld M (NULL: not written)
 };
 
 // ----------------------------------------------------------------- PTX glue
@@ -404,10 +416,11 @@ __host__ __device__ constexpr uint32_t idesc_e4m3(int bn) {
 //   STAGES    depth of the shared-memory ring (one 128-wide K block per stage)
 //   NBUF      TMEM partial-sum buffers (the MMA may run NBUF-1 K blocks ahead)
 //   EPI_WARPS promotion warps (a multiple of 4: one per TMEM lane quarter and slice)
-//   AQ        (swap only) the activations arrive as bf16 and are quantized by
-//             the kernel into a resident shared-memory operand; the ring
-//             carries only the weights
-template <int BN, bool SWAP, int STAGES, int NBUF, int EPI_WARPS, bool AQ = false>
+//   AQ        (swap only) 1: the activations arrive as bf16 and are quantized
+//             by the kernel into a resident shared-memory operand (the ring
+//             carries only the weights); 2: the same after an RMSNorm of
+//             each row, with the norm's side outputs
+template <int BN, bool SWAP, int STAGES, int NBUF, int EPI_WARPS, int AQ = 0>
 struct Cfg {
     static constexpr int kPBytes = kPRows * kBK;       // 16 KB
     static constexpr int kQBytes = AQ ? 0 : BN * kBK;
@@ -445,13 +458,11 @@ struct Cfg {
 // four units at a time per warp so that their latency chains (loads,
 // shuffles, the scale division) overlap.  The arithmetic is the norm+quant
 // kernels' (group_quant.cuh).
+// Rows [live, BN) of the resident operand: zero codes (whole 128-byte rows,
+// so the swizzle does not matter) and zero scales.
 template <int BN>
-__device__ __forceinline__ void quantize_activations(const Params& p, uint8_t* a_res, float* sa_slots,
-                                                     int slot_stride, int qw, int nw, int lane) {
-    constexpr int kU = 4;                       // units in flight per warp
-    const int KB = p.KB;
-    const int live = p.M < BN ? p.M : BN;
-    // Zero rows: bytes [live*128, BN*128) of every K block, and their scales.
+__device__ __forceinline__ void zero_rows(int KB, int live, uint8_t* a_res, float* sa_slots, int slot_stride, int qw,
+                                          int nw, int lane) {
     const int zero_vec = (BN - live) * (kBK / 16);          // uint4 per K block
     for (int e = qw * 32 + lane; e < KB * zero_vec; e += nw * 32) {
         const int kb = e / zero_vec, v = e % zero_vec;
@@ -462,6 +473,15 @@ __device__ __forceinline__ void quantize_activations(const Params& p, uint8_t* a
         sa_slots[kb * BN + r] = 0.f;
         sa_slots[slot_stride + kb * BN + r] = 0.f;
     }
+}
+
+template <int BN>
+__device__ __forceinline__ void quantize_activations(const Params& p, uint8_t* a_res, float* sa_slots,
+                                                     int slot_stride, int qw, int nw, int lane) {
+    constexpr int kU = 4;                       // units in flight per warp
+    const int KB = p.KB;
+    const int live = p.M < BN ? p.M : BN;
+    zero_rows<BN>(KB, live, a_res, sa_slots, slot_stride, qw, nw, lane);
     const int slots = (KB + 1) / 2;
     const int units = live * slots;
     const int h = lane >> 4;                    // half-warp h of slot i holds group 2i + h
@@ -513,6 +533,141 @@ __device__ __forceinline__ void quantize_activations(const Params& p, uint8_t* a
     }
 }
 
+// In-kernel RMSNorm + per-1x128 quantization of the decode rows (the fused
+// norm+quant of the q latent, then the GEMM, in one launch): warp qw takes
+// rows qw, qw + nw, ... whole, the row and gamma in registers, loaded in one
+// round.  The sum of squares is accumulated in the order of the warp-per-row
+// norm+quant kernel, r = 1/sqrt(ssq/K + eps) with IEEE operations,
+// x_hat = (x * r) * gamma in fp32, then the group quant of
+// quantize_activations, four slots at a time.  CTA 0 also writes the q codes
+// and scales when asked (the kv latent: norm_kv_rows, after the operand is
+// ready).  Splitting a row over several warps measured slower: the runtime
+// slot index sends the row to local memory.
+template <int BN>
+__device__ __forceinline__ void norm_quantize_activations(const Params& p, uint8_t* a_res, float* sa_slots,
+                                                          int slot_stride, int qw, int nw, int lane) {
+    constexpr int kMaxSlots = 8;                // 256 columns per slot: K <= 2048
+    constexpr int kU = 4;                       // slots quantized together
+    const int KB = p.KB;
+    const int live = p.M < BN ? p.M : BN;
+    zero_rows<BN>(KB, live, a_res, sa_slots, slot_stride, qw, nw, lane);
+    const int slots = (KB + 1) / 2;
+    const int h = lane >> 4;                    // half-warp h of slot i holds group 2i + h
+    const int c16 = (lane & 15) >> 1;
+    const bool side = blockIdx.x == 0;
+    const int K = KB * kBK;
+    for (int m = qw; m < live; m += nw) {
+        const __nv_bfloat16* row = p.a_bf16 + static_cast<int64_t>(m) * p.lda_bf16;
+        uint4 raw[kMaxSlots], graw[kMaxSlots];
+#pragma unroll
+        for (int i = 0; i < kMaxSlots; ++i) {
+            raw[i] = graw[i] = make_uint4(0, 0, 0, 0);
+            if (i < slots && 2 * i + h < KB) {
+                raw[i] = __ldg(reinterpret_cast<const uint4*>(row + (i * 32 + lane) * 8));
+                graw[i] = __ldg(reinterpret_cast<const uint4*>(p.gamma_q + (i * 32 + lane) * 8));
+            }
+        }
+        float2 sq[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+        for (int i = 0; i < kMaxSlots; ++i) {
+            if (i >= slots) break;
+            float2 x[4];
+            unpack8(raw[i], x);
+#pragma unroll
+            for (int t = 0; t < 4; ++t) sq[t & 1] = fma2(x[t], x[t], sq[t & 1]);
+        }
+        const float ssq = warp_sum((sq[0].x + sq[1].x) + (sq[0].y + sq[1].y));
+        const float r = 1.0f / sqrtf(ssq / p.kq_f + p.eps);   // correctly rounded sqrt and divide
+        const float2 r2 = make_float2(r, r);
+#pragma unroll
+        for (int i0 = 0; i0 < kMaxSlots; i0 += kU) {
+            if (i0 >= slots) break;
+            float2 x[kU][4];
+            float amax[kU];
+#pragma unroll
+            for (int j = 0; j < kU; ++j) {
+                float2 g[4];
+                unpack8(raw[i0 + j], x[j]);
+                unpack8(graw[i0 + j], g);
+#pragma unroll
+                for (int t = 0; t < 4; ++t) x[j][t] = mul2(mul2(x[j][t], r2), g[t]);
+                amax[j] = fmaxf(fmaxf(fmaxf(fabsf(x[j][0].x), fabsf(x[j][0].y)), fmaxf(fabsf(x[j][1].x), fabsf(x[j][1].y))),
+                                fmaxf(fmaxf(fabsf(x[j][2].x), fabsf(x[j][2].y)), fmaxf(fabsf(x[j][3].x), fabsf(x[j][3].y))));
+            }
+#pragma unroll
+            for (int o = 8; o > 0; o >>= 1) {
+#pragma unroll
+                for (int j = 0; j < kU; ++j) amax[j] = fmaxf(amax[j], __shfl_xor_sync(0xffffffffu, amax[j], o));
+            }
+#pragma unroll
+            for (int j = 0; j < kU; ++j) {
+                const int i = i0 + j, kb = 2 * i + h;
+                if (i >= slots || kb >= KB) continue;
+                const GroupQuant gq = make_group_quant(amax[j]);
+                bool ok;
+                uint2 codes = quant8_bracket(x[j], gq, ok);
+                if (!ok) codes = quant8_divide(x[j], gq.scale);
+                *reinterpret_cast<uint2*>(a_res + kb * (BN * kBK) + m * kBK + ((c16 ^ (m & 7)) << 4) + (lane & 1) * 8) =
+                    codes;
+                if ((lane & 15) == 0) {
+                    sa_slots[kb * BN + m] = gq.scale;
+                    sa_slots[slot_stride + kb * BN + m] = gq.scale;
+                }
+                if (side && p.q_out)
+                    *reinterpret_cast<uint2*>(p.q_out + static_cast<int64_t>(m) * K + (i * 32 + lane) * 8) = codes;
+                if (side && p.qs_out && (lane & 15) == 0) p.qs_out[static_cast<int64_t>(kb) * p.M + m] = gq.scale;
+            }
+        }
+    }
+}
+
+// The kv latent's rows of the fused call (CTA 0, after the q operand is
+// ready: off the GEMM's path): RMSNorm in the order of the warp-per-row
+// norm+quant kernel, bf16 out.
+__device__ __forceinline__ void norm_kv_rows(const Params& p, int qw, int nw, int lane) {
+    constexpr int kMaxSlots = 8;                // Kkv <= 2048
+    const int kchunks = p.kkv / 8;
+    for (int m = qw; m < p.M; m += nw) {
+        const __nv_bfloat16* krow = p.kv + static_cast<int64_t>(m) * p.ldkv;
+        uint4 raw[kMaxSlots], graw[kMaxSlots];
+#pragma unroll
+        for (int i = 0; i < kMaxSlots; ++i) {
+            raw[i] = graw[i] = make_uint4(0, 0, 0, 0);
+            if (i * 32 + lane < kchunks) {
+                raw[i] = __ldg(reinterpret_cast<const uint4*>(krow + (i * 32 + lane) * 8));
+                graw[i] = __ldg(reinterpret_cast<const uint4*>(p.gamma_kv + (i * 32 + lane) * 8));
+            }
+        }
+        float2 skv[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+        for (int i = 0; i < kMaxSlots; ++i) {
+            if (i * 32 >= kchunks) break;
+            float2 x[4];
+            unpack8(raw[i], x);
+#pragma unroll
+            for (int t = 0; t < 4; ++t) skv[t & 1] = fma2(x[t], x[t], skv[t & 1]);
+        }
+        const float ssq_kv = warp_sum((skv[0].x + skv[1].x) + (skv[0].y + skv[1].y));
+        const float rkv = 1.0f / sqrtf(ssq_kv / p.kkv_f + p.eps);
+        const float2 rk2 = make_float2(rkv, rkv);
+#pragma unroll
+        for (int i = 0; i < kMaxSlots; ++i) {
+            if (i * 32 + lane >= kchunks) continue;
+            float2 x[4], g[4];
+            unpack8(raw[i], x);
+            unpack8(graw[i], g);
+            uint4 v;
+            __nv_bfloat162* hv = reinterpret_cast<__nv_bfloat162*>(&v);
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                const float2 y = mul2(mul2(x[t], rk2), g[t]);
+                hv[t] = __floats2bfloat162_rn(y.x, y.y);
+            }
+            *reinterpret_cast<uint4*>(p.kv_out + static_cast<int64_t>(m) * p.ldkv_out + (i * 32 + lane) * 8) = v;
+        }
+    }
+}
+
 // Tile t of the concatenated tile space -> (problem, first activation row, first feature).
 // Activation tiles vary fastest, so CTAs running together share weight tiles in L2.
 template <int BN, bool SWAP>
@@ -524,7 +679,7 @@ __device__ __forceinline__ void tile_coords(const Params& p, int t, int& pi, int
     n0 = SWAP ? tn * kPRows : tn * BN;
 }
 
-template <int BN, bool SWAP, int STAGES, int NBUF, int EPI_WARPS, bool AQ = false>
+template <int BN, bool SWAP, int STAGES, int NBUF, int EPI_WARPS, int AQ = 0>
 __global__ void __launch_bounds__(Cfg<BN, SWAP, STAGES, NBUF, EPI_WARPS, AQ>::kThreads, 1)
 block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                          const __grid_constant__ CUtensorMap map_w0,
@@ -606,10 +761,15 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
     if (AQ && warp >= 2) {
         // Quantize the activations once for all of this CTA's tiles, while the
         // producer already streams weights into the ring.
-        quantize_activations<BN>(p, a_res, sa_slots, KBP * C::kScaleCols, warp - 2, C::kThreads / 32 - 2, lane);
+        if (AQ == 1)
+            quantize_activations<BN>(p, a_res, sa_slots, KBP * C::kScaleCols, warp - 2, C::kThreads / 32 - 2, lane);
+        else
+            norm_quantize_activations<BN>(p, a_res, sa_slots, KBP * C::kScaleCols, warp - 2, C::kThreads / 32 - 2,
+                                          lane);
         fence_proxy_async_smem();             // generic-proxy writes -> visible to the tensor core
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(aready));
+        if (AQ == 2 && blockIdx.x == 0) norm_kv_rows(p, warp - 2, C::kThreads / 32 - 2, lane);
     }
 
     if (warp == 0) {
@@ -916,7 +1076,7 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
     }
 }
 
-template <int BN, bool SWAP, int STAGES, int NBUF, int EPI_WARPS, bool AQ = false>
+template <int BN, bool SWAP, int STAGES, int NBUF, int EPI_WARPS, int AQ = 0>
 constexpr size_t smem_bytes(int KB) {
     using C = Cfg<BN, SWAP, STAGES, NBUF, EPI_WARPS, AQ>;
     const int KBP = (KB + 3) & ~3;
@@ -1562,7 +1722,7 @@ dsnq_status check_consumer(const Consumer& c, int64_t K) {
     return DSNQ_OK;
 }
 
-template <int BN, bool SWAP, int STAGES, int NBUF, int EPI_WARPS, bool AQ = false>
+template <int BN, bool SWAP, int STAGES, int NBUF, int EPI_WARPS, int AQ = 0>
 dsnq_status launch(gemm::Params& prm, const CUtensorMap& ma, const CUtensorMap& mw0, const CUtensorMap& mw1,
                    const CUtensorMap& mo0, const CUtensorMap& mo1, cudaStream_t stream) {
     using C = gemm::Cfg<BN, SWAP, STAGES, NBUF, EPI_WARPS, AQ>;
@@ -1615,11 +1775,28 @@ dsnq_status launch_pair(gemm::Params& prm, const CUtensorMap& ma, const CUtensor
     return launch_result(cudaLaunchKernelEx(&cfg, kern, ma, mw0, mw1, mo0, mo1, prm));
 }
 
+// The RMSNorm that precedes the in-kernel quantization, and its side
+// outputs (validated by the caller).
+struct NormSide {
+    const void* gamma_q;
+    const void* kv;
+    int64_t ldkv;
+    const void* gamma_kv;
+    int64_t kkv;
+    float eps;
+    void* kv_out;
+    int64_t ldkv_out;
+    void* q_out;
+    float* qs_out;
+};
+
 // a_bf16 != NULL selects the decode variant that quantizes bf16 activations
-// itself (see bf16a_in_gemm); a, as and the scale layout are then unused.
+// itself (see bf16a_in_gemm), after an RMSNorm when ns != NULL; a, as and the
+// scale layout are then unused.
 dsnq_status run_gemm(int64_t M, int64_t K, const void* a, int64_t lda, const float* as,
                      dsnq_scale_layout layout, int64_t ld_as, const Consumer& c0, const Consumer& c1,
-                     void* stream, const void* a_bf16 = nullptr, int64_t lda_bf16 = 0) {
+                     void* stream, const void* a_bf16 = nullptr, int64_t lda_bf16 = 0,
+                     const NormSide* ns = nullptr) {
     const bool aq = a_bf16 != nullptr;
     if (M < 0 || K <= 0 || c0.N < 0 || c1.N < 0) return DSNQ_ERR_INVALID_ARG;
     if (!aq && layout != DSNQ_SCALE_ROW_MAJOR && layout != DSNQ_SCALE_COL_MAJOR) return DSNQ_ERR_INVALID_ARG;
@@ -1666,6 +1843,20 @@ dsnq_status run_gemm(int64_t M, int64_t K, const void* a, int64_t lda, const flo
     prm.vec_scales = !aq && layout == DSNQ_SCALE_COL_MAJOR && ld % 4 == 0 && aligned(as, 16);
     prm.a_bf16 = static_cast<const __nv_bfloat16*>(a_bf16);
     prm.lda_bf16 = lda_bf16;
+    if (ns) {
+        prm.gamma_q = static_cast<const __nv_bfloat16*>(ns->gamma_q);
+        prm.kv = static_cast<const __nv_bfloat16*>(ns->kv);
+        prm.ldkv = ns->ldkv;
+        prm.gamma_kv = static_cast<const __nv_bfloat16*>(ns->gamma_kv);
+        prm.kkv = static_cast<int>(ns->kkv);
+        prm.kq_f = static_cast<float>(K);
+        prm.kkv_f = static_cast<float>(ns->kkv);
+        prm.eps = ns->eps;
+        prm.kv_out = static_cast<__nv_bfloat16*>(ns->kv_out);
+        prm.ldkv_out = ns->ldkv_out;
+        prm.q_out = static_cast<uint8_t*>(ns->q_out);
+        prm.qs_out = ns->qs_out;
+    }
     const int64_t rows_per_a_tile = swap ? bn : gemm::kPRows;
     prm.tiles_m = static_cast<int>((M + rows_per_a_tile - 1) / rows_per_a_tile);
 
@@ -1712,7 +1903,9 @@ dsnq_status run_gemm(int64_t M, int64_t K, const void* a, int64_t lda, const flo
     prm.inject = g_inject.load();
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (aq) return launch<16, true, 8, 32, 8, true>(prm, ma, mw[0], mw[1], mo[0], mo[1], s);
+    if (aq)
+        return ns ? launch<16, true, 8, 32, 8, 2>(prm, ma, mw[0], mw[1], mo[0], mo[1], s)
+                  : launch<16, true, 8, 32, 8, 1>(prm, ma, mw[0], mw[1], mo[0], mo[1], s);
     if (paired) return launch_pair(prm, ma, mw[0], mw[1], mo[0], mo[1], s);
     switch (bn) {
         // Decode: the MMA per K block is tiny, so the MMA <-> promotion round
@@ -1777,6 +1970,46 @@ extern "C" dsnq_status dsnq_block_scaled_fp8_gemm_dual_bf16a(
     st = dsnq_group_quant_bf16(M, K, a_bf16, lda, 128, a_fp8_ws, K, a_scale_ws, DSNQ_SCALE_COL_MAJOR, M, stream);
     if (st != DSNQ_OK) return st;
     return run_gemm(M, K, a_fp8_ws, K, a_scale_ws, DSNQ_SCALE_COL_MAJOR, M, c0, c1, stream);
+}
+
+extern "C" dsnq_status dsnq_fused_norm_quant_gemm_dual(
+    int64_t M, int64_t Kq, int64_t Kkv, const void* q, int64_t ldq, const void* kv, int64_t ldkv,
+    const void* gamma_q, const void* gamma_kv, float eps, void* kv_out, int64_t ldkv_out, int64_t N1,
+    const void* w1_fp8, int64_t ldw1, const float* w1_scale, int64_t ld_w1scale, void* out1_bf16, int64_t ldo1,
+    int64_t N2, const void* w2_fp8, int64_t ldw2, const float* w2_scale, int64_t ld_w2scale, void* out2_bf16,
+    int64_t ldo2, void* q_fp8, float* q_scale, void* stream) {
+    Consumer c0{N1, w1_fp8, ldw1, w1_scale, ld_w1scale, out1_bf16, ldo1};
+    Consumer c1{N2, w2_fp8, ldw2, w2_scale, ld_w2scale, out2_bf16, ldo2};
+    if (M < 0 || Kq <= 0 || Kkv <= 0 || N1 < 0 || N2 < 0) return DSNQ_ERR_INVALID_ARG;
+    if (!(eps >= 0.f) || eps > 3.4e38f) return DSNQ_ERR_INVALID_ARG;
+    if (Kq % 128 != 0 || Kkv % 8 != 0 || Kq / 8 + Kkv / 8 > 512) return DSNQ_ERR_UNSUPPORTED;
+    if (M == 0) return DSNQ_OK;
+    if (!q || !kv || !gamma_q || !gamma_kv || !kv_out) return DSNQ_ERR_INVALID_ARG;
+    if (ldq < Kq || ldkv < Kkv || ldkv_out < Kkv) return DSNQ_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(kv, 16) || !aligned(gamma_q, 16) || !aligned(gamma_kv, 16) ||
+        !aligned(kv_out, 16) || ldq % 8 || ldkv % 8 || ldkv_out % 8)
+        return DSNQ_ERR_MISALIGNED;
+    if ((q_fp8 && !aligned(q_fp8, 16)) || (q_scale && !aligned(q_scale, 4))) return DSNQ_ERR_MISALIGNED;
+    dsnq_status st = check_consumer(c0, Kq);
+    if (st != DSNQ_OK) return st;
+    st = check_consumer(c1, Kq);
+    if (st != DSNQ_OK) return st;
+    if (bf16a_in_gemm(M, Kq) && Kkv <= 2048) {
+        // A few decode rows: one launch normalizes, quantizes and multiplies.
+        const NormSide ns{gamma_q, kv, ldkv, gamma_kv, Kkv, eps, kv_out, ldkv_out, q_fp8, q_scale};
+        if (N1 == 0 && N2 == 0) {
+            // Nothing to multiply: the norm+quant alone (same outputs).
+            if (!q_fp8 || !q_scale) return DSNQ_ERR_INVALID_ARG;
+        } else {
+            return run_gemm(M, Kq, nullptr, 0, nullptr, DSNQ_SCALE_ROW_MAJOR, 0, c0, c1, stream, q, ldq, &ns);
+        }
+    }
+    // Otherwise the fused norm+quant kernel writes the pair, then the GEMM.
+    if (!q_fp8 || !q_scale) return DSNQ_ERR_INVALID_ARG;
+    st = dsnq_fused_dual_rmsnorm_group_quant(M, Kq, Kkv, q, ldq, kv, ldkv, gamma_q, gamma_kv, eps, 128, q_fp8, Kq,
+                                             q_scale, DSNQ_SCALE_COL_MAJOR, M, kv_out, ldkv_out, stream);
+    if (st != DSNQ_OK || (N1 == 0 && N2 == 0)) return st;
+    return run_gemm(M, Kq, q_fp8, Kq, q_scale, DSNQ_SCALE_COL_MAJOR, M, c0, c1, stream);
 }
 
 extern "C" dsnq_status dsnq_debug_status(void* stream) {

@@ -33,6 +33,13 @@ __device__ __forceinline__ uint32_t e4m3x2(float2 v) {
     return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(v, __NV_SATFINITE, __NV_E4M3));
 }
 
+// Sum over the 32 lanes (butterfly: every lane gets the same value).
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
 struct GroupQuant {
     float scale;            // amax / 448, IEEE fp32
     float2 ylo, yhi;        // fp32(1/scale) * (1 -+ 2^-20), rounded: bracket the quotient

@@ -125,12 +125,6 @@ __device__ __forceinline__ uint2 pack8_e4m3(const float2 (&f)[4], const QuantSca
     return make_uint2(quant4(f[0], f[1], qs), quant4(f[2], f[3], qs));
 }
 
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
-}
-
 __device__ __forceinline__ float half_warp_max(float v) {
 #pragma unroll
     for (int o = 8; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));

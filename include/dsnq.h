@@ -288,6 +288,40 @@ DSNQ_API dsnq_status dsnq_block_scaled_fp8_gemm_dual_bf16a(
     void* stream);
 
 /*
+ * The whole pre-projection in one call: the fused dual RMSNorm + per-1x128
+ * quant of dsnq_fused_dual_rmsnorm_group_quant, then the dual block-scaled
+ * GEMM of dsnq_block_scaled_fp8_gemm_dual on the quantized q latent.  Same
+ * formulas; kv_out as in the fused call.  No counterpart in the published
+ * method, which launches the two steps separately: for a few decode rows
+ * (M <= 16, Kq <= 2048, Kkv <= 2048 and M * ceil(Kq/256) <= 40, i.e. M <= 6
+ * at Kq = 1536) one launch normalizes and quantizes the rows inside the GEMM,
+ * where both steps are bound by latency; otherwise the fused norm+quant
+ * kernel writes (q_fp8, q_scale) and the GEMM reads them.
+ *   M, Kq, Kkv, q/ldq, kv/ldkv, gamma_q, gamma_kv, eps, kv_out/ldkv_out :
+ *                 as in dsnq_fused_dual_rmsnorm_group_quant.
+ *   consumers   : as in dsnq_block_scaled_fp8_gemm_dual (K = Kq).
+ *   q_fp8, q_scale : the quantized pair, e4m3 [M, Kq] with row stride Kq
+ *                 (16-byte aligned) and fp32 scales column-major with ld M
+ *                 (4-byte aligned).  Required outside the one-launch case
+ *                 (DSNQ_ERR_INVALID_ARG when NULL); there they are optional
+ *                 outputs (NULL: not written).
+ * Alignment and error rules as in the two calls it combines.
+ */
+DSNQ_API dsnq_status dsnq_fused_norm_quant_gemm_dual(
+    int64_t M, int64_t Kq, int64_t Kkv,
+    const void* q, int64_t ldq,
+    const void* kv, int64_t ldkv,
+    const void* gamma_q, const void* gamma_kv,
+    float eps,
+    void* kv_out, int64_t ldkv_out,
+    int64_t N1, const void* w1_fp8, int64_t ldw1, const float* w1_scale, int64_t ld_w1scale,
+    void* out1_bf16, int64_t ldo1,
+    int64_t N2, const void* w2_fp8, int64_t ldw2, const float* w2_scale, int64_t ld_w2scale,
+    void* out2_bf16, int64_t ldo2,
+    void* q_fp8, float* q_scale,
+    void* stream);
+
+/*
  * Device status word.  Kernels with bounded waits (the GEMM's mbarrier
  * waits) record a timeout there instead of hanging.  This call synchronizes
  * `stream`, reads the word of the current device, clears it and returns

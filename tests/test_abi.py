@@ -160,6 +160,29 @@ def test_bf16_activation_gemm_argument_checks(lib):
     assert call(lda=1540) == MISALIGNED
 
 
+def test_fused_norm_quant_gemm_argument_checks(lib):
+    f = lib.dsnq_fused_norm_quant_gemm_dual
+
+    def call(M=4, Kq=1536, Kkv=512, q=A, ldq=2112, kv=A + 3072, ldkv=2112, eps=1e-6, kvo=A, N1=512, qf=None, qs=None):
+        return f(M, Kq, Kkv, q, ldq, kv, ldkv, A, A, eps, kvo, Kkv, N1, A, Kq, A, Kq // 128, A, max(N1, 512),
+                 256, A, Kq, A, Kq // 128, A, 256, qf, qs, None)
+
+    assert call(M=0) == OK
+    assert call(M=-1) == INVALID
+    assert call(Kq=1000) == UNSUPPORTED
+    assert call(Kkv=100) == UNSUPPORTED
+    assert call(eps=float("nan")) == INVALID
+    assert call(eps=-1.0) == INVALID
+    assert call(q=None) == INVALID
+    assert call(kvo=None) == INVALID
+    assert call(ldq=1000) == INVALID
+    assert call(q=A + 8) == MISALIGNED
+    assert call(ldkv=2110) == MISALIGNED
+    assert call(qf=A + 8, qs=A) == MISALIGNED
+    assert call(N1=520) == UNSUPPORTED                     # N % 16
+    assert call(M=100) == INVALID                          # q_fp8 / q_scale needed above a few rows
+
+
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(_native, "_lib", None)
     monkeypatch.setattr(_native, "LIB_PATH", str(tmp_path / "libdsnq.so"))
