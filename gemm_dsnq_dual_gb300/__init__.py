@@ -31,7 +31,8 @@ __all__ = [
     "ROW_MAJOR", "COL_MAJOR", "DsnqError",
     "fused_dual_rmsnorm_group_quant", "rmsnorm_group_quant", "dual_rmsnorm_bf16", "group_quant_bf16",
     "quantize_weight_block128", "block_scaled_fp8_gemm", "block_scaled_fp8_gemm_dual",
-    "block_scaled_fp8_gemm_dual_bf16a", "fused_quant_fits", "fused_norm_quant_gemm_dual",
+    "block_scaled_fp8_gemm_dual_bf16a", "block_scaled_fp8_gemm_dual_bf16a_static", "fused_quant_fits",
+    "fused_norm_quant_gemm_dual",
     "quant_output_sizes", "debug_status", "debug_set", "set_launch_overlap", "scale_layout_of", "scale_ld_for",
     "empty_scales",
 ]
@@ -252,6 +253,27 @@ def block_scaled_fp8_gemm_dual_bf16a(a_bf16, w1_fp8, w1_scale, w2_fp8, w2_scale,
         N2, w2_fp8.data_ptr(), _row_view_ok(w2_fp8, "w2_fp8"), w2_scale.data_ptr(),
         _row_view_ok(w2_scale, "w2_scale"), out2.data_ptr(), _row_view_ok(out2, "out2"),
         ws_a, ws_s, _stream(stream)), "dsnq_block_scaled_fp8_gemm_dual_bf16a")
+    return out1, out2
+
+
+def block_scaled_fp8_gemm_dual_bf16a_static(a_bf16, w1_fp8, w1_scale, w2_fp8, w2_scale,
+                                            out1=None, out2=None, stream=None):
+    """block_scaled_fp8_gemm_dual_bf16a with the library's own device scratch
+    (M, K <= 2048): nothing is allocated for the quantized pair."""
+    M, K = a_bf16.shape
+    N1, N2 = w1_fp8.shape[0], w2_fp8.shape[0]
+    dev = a_bf16.device
+    if out1 is None:
+        out1 = torch.empty(M, N1, dtype=torch.bfloat16, device=dev)
+    if out2 is None:
+        out2 = torch.empty(M, N2, dtype=torch.bfloat16, device=dev)
+    check(lib().dsnq_block_scaled_fp8_gemm_dual_bf16a_static(
+        M, K, a_bf16.data_ptr(), _row_view_ok(a_bf16, "a_bf16"),
+        N1, w1_fp8.data_ptr(), _row_view_ok(w1_fp8, "w1_fp8"), w1_scale.data_ptr(),
+        _row_view_ok(w1_scale, "w1_scale"), out1.data_ptr(), _row_view_ok(out1, "out1"),
+        N2, w2_fp8.data_ptr(), _row_view_ok(w2_fp8, "w2_fp8"), w2_scale.data_ptr(),
+        _row_view_ok(w2_scale, "w2_scale"), out2.data_ptr(), _row_view_ok(out2, "out2"),
+        _stream(stream)), "dsnq_block_scaled_fp8_gemm_dual_bf16a_static")
     return out1, out2
 
 

@@ -46,6 +46,11 @@ SIGNATURES = {
               i64, vp, i64, vp, i64, vp, i64,
               i64, vp, i64, vp, i64, vp, i64,
               vp, vp, vp]),
+    "dsnq_block_scaled_fp8_gemm_dual_bf16a_static": (
+        i32, [i64, i64, vp, i64,
+              i64, vp, i64, vp, i64, vp, i64,
+              i64, vp, i64, vp, i64, vp, i64,
+              vp]),
     "dsnq_block_scaled_fp8_gemm_dual_bf16a": (
         i32, [i64, i64, vp, i64,
               i64, vp, i64, vp, i64, vp, i64,

@@ -24,7 +24,7 @@ BUILD_DIR = os.path.join(ROOT, "_build", platform.machine() or "unknown")
 LIB_NAME = "libdsnq.so"
 LIB_PATH = os.path.join(PKG_DIR, LIB_NAME)
 
-SOURCES = ["norm_quant.cu", "gemm_fp8.cu", "dsnq_api.cu"]
+SOURCES = ["norm_quant.cu", "gemm_fp8.cu", "dsnq_api.cu", "static_scratch.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "--expt-relaxed-constexpr",
          "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
@@ -50,7 +50,7 @@ def _newer(target: str, deps) -> bool:
 
 def _headers():
     hs = [os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE) if f.endswith(".h")]
-    hs += [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".h")]
+    hs += [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".h", ".cuh"))]
     return hs
 
 

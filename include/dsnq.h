@@ -288,6 +288,25 @@ DSNQ_API dsnq_status dsnq_block_scaled_fp8_gemm_dual_bf16a(
     void* stream);
 
 /*
+ * dsnq_block_scaled_fp8_gemm_dual_bf16a without a workspace argument: the
+ * quantized pair goes to a device array inside the library (2048 x 2048
+ * codes and their scales), so the call allocates nothing.  No counterpart in
+ * the published method: an interface variant of this implementation.
+ * M <= 2048 and K <= 2048 (DSNQ_ERR_UNSUPPORTED otherwise); other arguments
+ * and rules as in dsnq_block_scaled_fp8_gemm_dual_bf16a.  Calls that use the
+ * array (those outside the one-launch case) share it: on one device they must
+ * be ordered, e.g. issued to one stream.
+ */
+DSNQ_API dsnq_status dsnq_block_scaled_fp8_gemm_dual_bf16a_static(
+    int64_t M, int64_t K,
+    const void* a_bf16, int64_t lda,
+    int64_t N1, const void* w1_fp8, int64_t ldw1, const float* w1_scale, int64_t ld_w1scale,
+    void* out1_bf16, int64_t ldo1,
+    int64_t N2, const void* w2_fp8, int64_t ldw2, const float* w2_scale, int64_t ld_w2scale,
+    void* out2_bf16, int64_t ldo2,
+    void* stream);
+
+/*
  * The whole pre-projection in one call: the fused dual RMSNorm + per-1x128
  * quant of dsnq_fused_dual_rmsnorm_group_quant, then the dual block-scaled
  * GEMM of dsnq_block_scaled_fp8_gemm_dual on the quantized q latent.  Same

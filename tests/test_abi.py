@@ -160,6 +160,18 @@ def test_bf16_activation_gemm_argument_checks(lib):
     assert call(lda=1540) == MISALIGNED
 
 
+def test_static_scratch_gemm_argument_checks(lib):
+    f = lib.dsnq_block_scaled_fp8_gemm_dual_bf16a_static
+
+    def call(M=4, K=1536):
+        return f(M, K, A, K, 512, A, K, A, K // 128, A, 512, 256, A, K, A, K // 128, A, 256, None)
+
+    assert call(M=0) == OK
+    assert call(M=-1) == INVALID
+    assert call(M=2049) == UNSUPPORTED                     # beyond the library's scratch
+    assert call(K=2176) == UNSUPPORTED
+
+
 def test_fused_norm_quant_gemm_argument_checks(lib):
     f = lib.dsnq_fused_norm_quant_gemm_dual
 

@@ -1,0 +1,43 @@
+"""The bf16-activation dual GEMM with the library's own device scratch for
+the quantized pair (no workspace argument, nothing allocated): same results
+as the call with a caller workspace, bit for bit, on both routes (quantized
+inside the GEMM for a few rows; quant kernel, then the GEMM, above), and
+parity with the oracle."""
+
+import pytest
+import torch
+
+import oracle
+import gemm_dsnq_dual_gb300 as dsnq
+from gemm_dsnq_dual_gb300 import inputs
+from parity import GEMM_REL_FRO, bf16_value, rel_fro
+
+pytestmark = pytest.mark.gpu
+
+
+def weights(K):
+    out = []
+    for N, seed in ((512, 91), (256, 92)):
+        wc, ws = oracle.quantize_weight_block128(inputs.weight(N, K, seed=seed).numpy())
+        out += [wc, ws]
+    return out
+
+
+@pytest.mark.parametrize("M,K", [(1, 1536), (7, 1536), (300, 1536), (2048, 2048)])
+def test_static_scratch_equals_workspace(M, K):
+    a = inputs.activations_bf16(M, K, seed=93 + M).cuda()
+    w1, s1, w2, s2 = weights(K)
+    W = [torch.from_numpy(x).cuda() for x in (w1, s1, w2, s2)]
+    o1 = torch.empty(M, 512, dtype=torch.bfloat16, device="cuda")
+    o2 = torch.empty(M, 256, dtype=torch.bfloat16, device="cuda")
+    torch.cuda.synchronize()
+    before = torch.cuda.memory_allocated()
+    dsnq.block_scaled_fp8_gemm_dual_bf16a_static(a, *W, out1=o1, out2=o2)
+    torch.cuda.synchronize()
+    assert torch.cuda.memory_allocated() == before       # no tensor allocated for the call
+    r1, r2 = dsnq.block_scaled_fp8_gemm_dual_bf16a(a, *W)
+    assert torch.equal(o1, r1) and torch.equal(o2, r2)
+    if M == 300:
+        codes, scale = oracle.group_quant_bf16(inputs.bits(a.cpu()))
+        ref = oracle.block_scaled_gemm(codes, scale, w1, s1)
+        assert rel_fro(bf16_value(o1), ref) <= GEMM_REL_FRO
