@@ -299,9 +299,8 @@ def fused_norm_quant_gemm_dual(q, kv, gamma_q, gamma_kv, eps, w1_fp8, w1_scale, 
             q_fp8 = torch.empty(M, Kq, dtype=torch.float8_e4m3fn, device=dev)
         if q_scale is None:
             q_scale = empty_scales(M, Kq // GROUP, COL_MAJOR, dev)
-    for t, name in ((q_fp8, "q_fp8"), (q_scale, "q_scale")):
-        if t is not None and name == "q_fp8" and not t.is_contiguous():
-            raise ValueError("q_fp8 must be contiguous [M, Kq]")
+    if q_fp8 is not None and not q_fp8.is_contiguous():
+        raise ValueError("q_fp8 must be contiguous [M, Kq]")
     if q_scale is not None and M > 1 and q_scale.stride() != (1, M):
         raise ValueError("q_scale must be column-major [M, Kq/128] (strides (1, M))")
     check(lib().dsnq_fused_norm_quant_gemm_dual(
