@@ -1,5 +1,7 @@
 // W8A8 block-scaled FP8 GEMM on pre-quantized activations, tcgen05 + TMA +
-// TMEM, for one or two consumers of the same activation.
+// TMEM, for one or two consumers of the same activation; and, for a few
+// decode rows, the same GEMM on bf16 activations that the kernel quantizes
+// (or normalizes and quantizes) itself in its prologue.
 //
 //   out[m, n] = bf16( sum_kb sa(m, kb) * sw[n/128, kb] * sum_{k in kb} a[m,k] w[n,k] )
 //
@@ -36,6 +38,9 @@
 //     wasted on padding and the kernel streams the weights.
 //   * Dual consumer: the tile index space of both problems is concatenated
 //     into one launch; both read the same activation tensor map.
+//   * bf16 activations (decode variant AQ = 1, or 2 with an RMSNorm first):
+//     warps 2.. quantize the rows into a resident shared-memory operand before
+//     taking up their roles, and the ring carries only the weights.
 //   * Every wait is bounded (globaltimer); on expiry the kernel records a
 //     timeout in the device status word, drains its own copies and MMAs with
 //     bounded waits, frees its TMEM and returns.
