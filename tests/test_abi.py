@@ -160,6 +160,19 @@ def test_bf16_activation_gemm_argument_checks(lib):
     assert call(lda=1540) == MISALIGNED
 
 
+def test_python_and_library_agree_on_the_in_gemm_route(lib):
+    """With a misaligned lda and no workspace, the in-GEMM route reports
+    MISALIGNED and the two-launch route reports the missing workspace
+    (INVALID): the library's dispatch is visible without a GPU."""
+    import gemm_dsnq_dual_gb300 as dsnq
+    f = lib.dsnq_block_scaled_fp8_gemm_dual_bf16a
+    for K in range(128, 2048 + 256, 128):
+        for M in range(1, 21):
+            st = f(M, K, A, K + 4, 512, A, K, A, K // 128, A, 512, 0, None, 0, None, 0, None, 0, None, None, None)
+            assert st in (MISALIGNED, INVALID), (M, K, st)
+            assert (st == MISALIGNED) == dsnq.fused_quant_fits(M, K), (M, K)
+
+
 def test_static_scratch_gemm_argument_checks(lib):
     f = lib.dsnq_block_scaled_fp8_gemm_dual_bf16a_static
 
