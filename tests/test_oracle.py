@@ -219,6 +219,25 @@ def test_fused_single_rounding_is_at_least_as_accurate():
 
 # ------------------------------------------------------------------ GEMM
 
+def test_bf16_group_quant_matches_torch_fp32_quotient_and_cast():
+    """The quant of bf16 activations (baseline step 2, and the GEMM on bf16
+    activations): scale = fp32 division amax / 448 and code = torch's e4m3
+    cast of the fp32 quotient x / scale, computed entirely by torch."""
+    g = torch.Generator().manual_seed(12)
+    x = (torch.randn(64, 1536, generator=g) * torch.exp2(torch.randint(-6, 6, (64, 1, 1536 // 128), generator=g)
+                                                          .float().repeat_interleave(128, dim=2).squeeze(1)))
+    x[3] = 0.0                                                   # an all-zero row
+    xb = x.to(torch.bfloat16)
+    codes, scale = oracle.group_quant_bf16(inputs.bits(xb))
+    x32 = xb.float().view(64, 12, 128)
+    amax = x32.abs().amax(dim=2)
+    s32 = amax / torch.tensor(448.0)                             # IEEE fp32 division
+    q = torch.where(s32[..., None] > 0, x32 / s32[..., None].clamp_min(torch.finfo(torch.float32).tiny), x32 * 0)
+    want_codes = q.to(torch.float8_e4m3fn).view(torch.uint8).reshape(64, 1536).numpy()
+    assert np.array_equal(scale, s32.numpy())
+    assert np.array_equal(codes, want_codes)
+
+
 def test_weight_block_quant_properties():
     w = inputs.weight(300, 256, seed=1).numpy()       # ragged N: 3 blocks, last 44 rows
     codes, sw = oracle.quantize_weight_block128(w)
