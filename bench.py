@@ -14,12 +14,18 @@ The JSON line also reports, measured in the same run:
   * per-kernel times and roofline fractions (GEMM vs the FP8 tensor peak,
     norm+quant vs HBM bandwidth), against MEASURED_PEAKS.json when present;
   * the norm+quant latency at M=1 (decode), from a CUDA graph of 100 calls on
-    100 cold rows, and its GB/s at M=1024/8192/32768;
+    100 cold rows (with launch overlap on and off), and its GB/s at
+    M=1024/8192/32768;
+  * one decode step at M=1 (norm+quant, then the dual GEMM over cold
+    weights): two launches with and without launch overlap, the one-launch
+    call, and the dual GEMM on a bf16 row quantized inside the GEMM or by the
+    quant kernel first;
+  * the dual GEMM alone over decode and larger batch sizes;
   * the unfused three-kernel sequence (dual RMSNorm to bf16, then the per-1x128
     quant twice) on the same GPU at the same M;
   * e2e: the same step through the public API with pinned host buffers
     (inputs copied in, both projections and kv copied out, inside the timer);
-  * cpu_baseline: the fp64 CPU oracle timed on a bounded sample of rows.
+  * cpu_baseline: the fp64 CPU oracle timed on the whole M=8192 workload.
 
 `--impl reference` times the CPU oracle alone on the same metric (bounded
 samples of rows and output columns so the run ends within minutes).
