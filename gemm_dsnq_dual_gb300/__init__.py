@@ -32,15 +32,25 @@ __all__ = [
     "fused_dual_rmsnorm_group_quant", "rmsnorm_group_quant", "dual_rmsnorm_bf16", "group_quant_bf16",
     "quantize_weight_block128", "block_scaled_fp8_gemm", "block_scaled_fp8_gemm_dual",
     "block_scaled_fp8_gemm_dual_bf16a", "block_scaled_fp8_gemm_dual_bf16a_static", "fused_quant_fits",
+    "bf16a_workspace_bytes", "gemm_plan",
     "fused_norm_quant_gemm_dual",
     "quant_output_sizes", "debug_status", "debug_set", "set_launch_overlap", "scale_layout_of", "scale_ld_for",
     "empty_scales",
 ]
 
 
-def _stream(stream) -> int:
+def _stream(stream, dev) -> int:
+    """The stream handle for a call on tensors of device `dev`.  The library
+    launches on the current CUDA device (and picks per-device state by it), so
+    tensors on another device are refused rather than silently mixed."""
+    if dev.type != "cuda":
+        raise ValueError(f"tensors must be CUDA tensors, got {dev}")
+    cur = torch.cuda.current_device()
+    if dev.index is not None and dev.index != cur:
+        raise ValueError(f"tensors are on {dev} but the current CUDA device is cuda:{cur}; "
+                         f"call under torch.cuda.device({dev})")
     if stream is None:
-        stream = torch.cuda.current_stream()
+        stream = torch.cuda.current_stream(cur)
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
 
@@ -119,7 +129,7 @@ def fused_dual_rmsnorm_group_quant(q, kv, gamma_q, gamma_kv, eps: float = 1e-6, 
         M, Kq, Kkv, q.data_ptr(), _row_view_ok(q, "q"), kv.data_ptr(), _row_view_ok(kv, "kv"),
         gamma_q.data_ptr(), gamma_kv.data_ptr(), float(eps), group,
         q_out.data_ptr(), _row_view_ok(q_out, "q_out"), q_scale.data_ptr(), lay, ld,
-        kv_out.data_ptr(), _row_view_ok(kv_out, "kv_out"), _stream(stream)),
+        kv_out.data_ptr(), _row_view_ok(kv_out, "kv_out"), _stream(stream, q.device)),
         "dsnq_fused_dual_rmsnorm_group_quant")
     return q_out, q_scale, kv_out
 
@@ -137,7 +147,7 @@ def rmsnorm_group_quant(x, gamma, eps: float = 1e-6, group: int = GROUP, scale_l
     ld = scale_ld_for(x_scale, lay)
     check(lib().dsnq_rmsnorm_group_quant(
         M, K, x.data_ptr(), _row_view_ok(x, "x"), gamma.data_ptr(), float(eps), group,
-        x_out.data_ptr(), _row_view_ok(x_out, "x_out"), x_scale.data_ptr(), lay, ld, _stream(stream)),
+        x_out.data_ptr(), _row_view_ok(x_out, "x_out"), x_scale.data_ptr(), lay, ld, _stream(stream, x.device)),
         "dsnq_rmsnorm_group_quant")
     return x_out, x_scale
 
@@ -154,7 +164,7 @@ def dual_rmsnorm_bf16(q, kv, gamma_q, gamma_kv, eps: float = 1e-6, q_out=None, k
         M, Kq, Kkv, q.data_ptr(), _row_view_ok(q, "q"), kv.data_ptr(), _row_view_ok(kv, "kv"),
         gamma_q.data_ptr(), gamma_kv.data_ptr(), float(eps),
         q_out.data_ptr(), _row_view_ok(q_out, "q_out"), kv_out.data_ptr(), _row_view_ok(kv_out, "kv_out"),
-        _stream(stream)), "dsnq_dual_rmsnorm_bf16")
+        _stream(stream, q.device)), "dsnq_dual_rmsnorm_bf16")
     return q_out, kv_out
 
 
@@ -169,7 +179,7 @@ def group_quant_bf16(x, group: int = GROUP, scale_layout=ROW_MAJOR, x_out=None, 
     ld = scale_ld_for(x_scale, lay)
     check(lib().dsnq_group_quant_bf16(
         M, K, x.data_ptr(), _row_view_ok(x, "x"), group, x_out.data_ptr(), _row_view_ok(x_out, "x_out"),
-        x_scale.data_ptr(), lay, ld, _stream(stream)), "dsnq_group_quant_bf16")
+        x_scale.data_ptr(), lay, ld, _stream(stream, x.device)), "dsnq_group_quant_bf16")
     return x_out, x_scale
 
 
@@ -182,7 +192,7 @@ def quantize_weight_block128(w, w_out=None, w_scale=None, stream=None):
         w_scale = torch.empty((N + 127) // 128, K // 128, dtype=torch.float32, device=w.device)
     check(lib().dsnq_quantize_weight_block128(
         N, K, w.data_ptr(), _row_view_ok(w, "w"), w_out.data_ptr(), _row_view_ok(w_out, "w_out"),
-        w_scale.data_ptr(), _row_view_ok(w_scale, "w_scale"), _stream(stream)),
+        w_scale.data_ptr(), _row_view_ok(w_scale, "w_scale"), _stream(stream, w.device)),
         "dsnq_quantize_weight_block128")
     return w_out, w_scale
 
@@ -197,7 +207,7 @@ def block_scaled_fp8_gemm(a_fp8, a_scale, w_fp8, w_scale, out=None, stream=None)
     check(lib().dsnq_block_scaled_fp8_gemm(
         M, N, K, a_fp8.data_ptr(), _row_view_ok(a_fp8, "a_fp8"), a_scale.data_ptr(), lay, ld,
         w_fp8.data_ptr(), _row_view_ok(w_fp8, "w_fp8"), w_scale.data_ptr(), _row_view_ok(w_scale, "w_scale"),
-        out.data_ptr(), _row_view_ok(out, "out"), _stream(stream)), "dsnq_block_scaled_fp8_gemm")
+        out.data_ptr(), _row_view_ok(out, "out"), _stream(stream, a_fp8.device)), "dsnq_block_scaled_fp8_gemm")
     return out
 
 
@@ -218,14 +228,32 @@ def block_scaled_fp8_gemm_dual(a_fp8, a_scale, w1_fp8, w1_scale, w2_fp8, w2_scal
         _row_view_ok(w1_scale, "w1_scale"), out1.data_ptr(), _row_view_ok(out1, "out1"),
         N2, w2_fp8.data_ptr(), _row_view_ok(w2_fp8, "w2_fp8"), w2_scale.data_ptr(),
         _row_view_ok(w2_scale, "w2_scale"), out2.data_ptr(), _row_view_ok(out2, "out2"),
-        _stream(stream)), "dsnq_block_scaled_fp8_gemm_dual")
+        _stream(stream, a_fp8.device)), "dsnq_block_scaled_fp8_gemm_dual")
     return out1, out2
+
+
+def bf16a_workspace_bytes(M: int, K: int):
+    """(code_bytes, scale_bytes) of the workspace block_scaled_fp8_gemm_dual_bf16a
+    needs for M rows of K bf16 activations; (0, 0) when it quantizes inside
+    the GEMM (the library's own rule, dsnq_bf16a_workspace_bytes)."""
+    c, s = C.c_int64(), C.c_int64()
+    check(lib().dsnq_bf16a_workspace_bytes(M, K, C.byref(c), C.byref(s)), "dsnq_bf16a_workspace_bytes")
+    return c.value, s.value
 
 
 def fused_quant_fits(M: int, K: int) -> bool:
     """True when block_scaled_fp8_gemm_dual_bf16a quantizes inside the GEMM
     (one launch, no workspace)."""
-    return 0 < M <= 16 and K <= 2048 and M * ((K // 128 + 1) // 2) <= 40
+    return M > 0 and bf16a_workspace_bytes(M, K) == (0, 0)
+
+
+def gemm_plan(M: int, K: int):
+    """(variant, dynamic shared memory bytes) of the GEMM kernel that
+    block_scaled_fp8_gemm(_dual) launches for M rows and reduction length K
+    (host-only query, dsnq_gemm_plan)."""
+    v, b = C.c_int32(), C.c_int64()
+    check(lib().dsnq_gemm_plan(M, K, C.byref(v), C.byref(b)), "dsnq_gemm_plan")
+    return v.value, b.value
 
 
 def block_scaled_fp8_gemm_dual_bf16a(a_bf16, w1_fp8, w1_scale, w2_fp8, w2_scale,
@@ -241,10 +269,11 @@ def block_scaled_fp8_gemm_dual_bf16a(a_bf16, w1_fp8, w1_scale, w2_fp8, w2_scale,
     if out2 is None:
         out2 = torch.empty(M, N2, dtype=torch.bfloat16, device=dev)
     ws_a = ws_s = 0
-    if M > 0 and not fused_quant_fits(M, K):
+    code_bytes, scale_bytes = bf16a_workspace_bytes(M, K)
+    if code_bytes:
         if workspace is None:
-            workspace = (torch.empty(M, K, dtype=torch.uint8, device=dev),
-                         torch.empty(M * (K // GROUP), dtype=torch.float32, device=dev))
+            workspace = (torch.empty(code_bytes, dtype=torch.uint8, device=dev),
+                         torch.empty(scale_bytes // 4, dtype=torch.float32, device=dev))
         ws_a, ws_s = workspace[0].data_ptr(), workspace[1].data_ptr()
     check(lib().dsnq_block_scaled_fp8_gemm_dual_bf16a(
         M, K, a_bf16.data_ptr(), _row_view_ok(a_bf16, "a_bf16"),
@@ -252,7 +281,7 @@ def block_scaled_fp8_gemm_dual_bf16a(a_bf16, w1_fp8, w1_scale, w2_fp8, w2_scale,
         _row_view_ok(w1_scale, "w1_scale"), out1.data_ptr(), _row_view_ok(out1, "out1"),
         N2, w2_fp8.data_ptr(), _row_view_ok(w2_fp8, "w2_fp8"), w2_scale.data_ptr(),
         _row_view_ok(w2_scale, "w2_scale"), out2.data_ptr(), _row_view_ok(out2, "out2"),
-        ws_a, ws_s, _stream(stream)), "dsnq_block_scaled_fp8_gemm_dual_bf16a")
+        ws_a, ws_s, _stream(stream, a_bf16.device)), "dsnq_block_scaled_fp8_gemm_dual_bf16a")
     return out1, out2
 
 
@@ -273,7 +302,7 @@ def block_scaled_fp8_gemm_dual_bf16a_static(a_bf16, w1_fp8, w1_scale, w2_fp8, w2
         _row_view_ok(w1_scale, "w1_scale"), out1.data_ptr(), _row_view_ok(out1, "out1"),
         N2, w2_fp8.data_ptr(), _row_view_ok(w2_fp8, "w2_fp8"), w2_scale.data_ptr(),
         _row_view_ok(w2_scale, "w2_scale"), out2.data_ptr(), _row_view_ok(out2, "out2"),
-        _stream(stream)), "dsnq_block_scaled_fp8_gemm_dual_bf16a_static")
+        _stream(stream, a_bf16.device)), "dsnq_block_scaled_fp8_gemm_dual_bf16a_static")
     return out1, out2
 
 
@@ -311,13 +340,13 @@ def fused_norm_quant_gemm_dual(q, kv, gamma_q, gamma_kv, eps, w1_fp8, w1_scale, 
         N2, w2_fp8.data_ptr(), _row_view_ok(w2_fp8, "w2_fp8"), w2_scale.data_ptr(),
         _row_view_ok(w2_scale, "w2_scale"), out2.data_ptr(), _row_view_ok(out2, "out2"),
         0 if q_fp8 is None else q_fp8.data_ptr(), 0 if q_scale is None else q_scale.data_ptr(),
-        _stream(stream)), "dsnq_fused_norm_quant_gemm_dual")
+        _stream(stream, q.device)), "dsnq_fused_norm_quant_gemm_dual")
     return out1, out2, kv_out, q_fp8, q_scale
 
 
 def debug_status(stream=None) -> int:
     """Synchronizes the stream and returns (and clears) the device status."""
-    return lib().dsnq_debug_status(_stream(stream))
+    return lib().dsnq_debug_status(_stream(stream, torch.device("cuda", torch.cuda.current_device())))
 
 
 def debug_set(inject_flags: int = 0, wait_timeout_ns: int = 0) -> None:

@@ -56,6 +56,8 @@ SIGNATURES = {
               i64, vp, i64, vp, i64, vp, i64,
               i64, vp, i64, vp, i64, vp, i64,
               vp, vp, vp]),
+    "dsnq_gemm_plan": (i32, [i64, i64, C.POINTER(C.c_int32), pi64]),
+    "dsnq_bf16a_workspace_bytes": (i32, [i64, i64, pi64, pi64]),
     "dsnq_debug_status": (i32, [vp]),
     "dsnq_debug_set": (None, [u32, u64]),
     "dsnq_set_launch_overlap": (None, [i32]),

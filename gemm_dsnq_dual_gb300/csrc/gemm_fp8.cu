@@ -192,6 +192,15 @@ __device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, uint64
     }
 }
 
+// Lets `ns` nanoseconds pass (abort path only): long enough for any bulk
+// copy already issued to land, when there is no barrier this thread can
+// watch for it.
+constexpr uint64_t kAbortSettleNs = 200000;
+__device__ __forceinline__ void settle_ns(uint64_t ns) {
+    const uint64_t t0 = now_ns();
+    while (now_ns() - t0 < ns) __nanosleep(1000);
+}
+
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
                                             int32_t x, int32_t y) {
     asm volatile(
@@ -215,6 +224,18 @@ __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wa
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+
+// Tiled bulk prefetch of a tensor tile into L2 (no shared memory, no barrier).
+__device__ __forceinline__ void tma_prefetch_l2(const CUtensorMap* map, int32_t x, int32_t y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y)
+                 : "memory");
+}
+
+// K blocks of weight tiles a decode CTA prefetches into L2 before waiting
+// for the previous kernel of its stream (16 KB each).
+constexpr int kPrefetchKBlocks = 24;
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
@@ -541,8 +562,9 @@ __device__ __forceinline__ void quantize_activations(const Params& p, uint8_t* a
 // In-kernel RMSNorm + per-1x128 quantization of the decode rows (the fused
 // norm+quant of the q latent, then the GEMM, in one launch): warp qw takes
 // rows qw, qw + nw, ... whole, the row and gamma in registers, loaded in one
-// round.  The sum of squares is accumulated in the order of the warp-per-row
-// norm+quant kernel, r = 1/sqrt(ssq/K + eps) with IEEE operations,
+// round.  The sum of squares is accumulated per lane in two fp32 pairs and
+// summed across the warp by a butterfly, r = 1/sqrt(ssq/K + eps) with IEEE
+// operations,
 // x_hat = (x * r) * gamma in fp32, then the group quant of
 // quantize_activations, four slots at a time.  CTA 0 also writes the q codes
 // and scales when asked (the kv latent: norm_kv_rows, after the operand is
@@ -627,8 +649,7 @@ __device__ __forceinline__ void norm_quantize_activations(const Params& p, uint8
 }
 
 // The kv latent's rows of the fused call (CTA 0, after the q operand is
-// ready: off the GEMM's path): RMSNorm in the order of the warp-per-row
-// norm+quant kernel, bf16 out.
+// ready: off the GEMM's path): RMSNorm as for the q rows above, bf16 out.
 __device__ __forceinline__ void norm_kv_rows(const Params& p, int qw, int nw, int lane) {
     constexpr int kMaxSlots = 8;                // Kkv <= 2048
     const int kchunks = p.kkv / 8;
@@ -684,8 +705,8 @@ __device__ __forceinline__ void tile_coords(const Params& p, int t, int& pi, int
     n0 = SWAP ? tn * kPRows : tn * BN;
 }
 
-template <int BN, bool SWAP, int STAGES, int NBUF, int EPI_WARPS, int AQ = 0>
-__global__ void __launch_bounds__(Cfg<BN, SWAP, STAGES, NBUF, EPI_WARPS, AQ>::kThreads, 1)
+template <int BN, bool SWAP, int STAGES, int NBUF, int EPI_WARPS, int AQ = 0, int MINB = 1>
+__global__ void __launch_bounds__(Cfg<BN, SWAP, STAGES, NBUF, EPI_WARPS, AQ>::kThreads, MINB)
 block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                          const __grid_constant__ CUtensorMap map_w0,
                          const __grid_constant__ CUtensorMap map_w1,
@@ -758,6 +779,23 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
     const uint64_t tmo = p.timeout_ns;
+    if (SWAP && warp == 0) {
+        // Decode: the weight tiles of this CTA's first K blocks into L2 while
+        // the previous kernel of the stream may still run (the weights are
+        // the whole stream at decode sizes).  A prefetch only moves data into
+        // L2, the point of coherence of global memory, so it cannot make a
+        // later load read stale data even if an earlier kernel writes the
+        // weights; the loads themselves still wait below.  (The same prefetch
+        // in the 128 x 128 and CTA-pair kernels measured slower.)
+        const int cap = kPrefetchKBlocks;
+        int done = 0;
+        for (int t = blockIdx.x; t < total && done < cap; t += gridDim.x, done += KB) {
+            int pi, m0, n0;
+            tile_coords<BN, SWAP>(p, t, pi, m0, n0);
+            for (int kb = lane; kb < KB && done + kb < cap; kb += 32)
+                tma_prefetch_l2(pi ? &map_w1 : &map_w0, kb * kBK, n0);
+        }
+    }
     // Everything above reads no argument buffer; from here on every role
     // reads inputs (or writes outputs that an earlier kernel may still read).
     grid_dependency_wait();
@@ -1345,7 +1383,16 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
                 const uint32_t gn = last - 1 + kStages;
                 ok = wait_bounded(smem_u32(&empty[s]), ((gn / kStages) & 1) ^ 1, abort_flag, tmo);
             }
-            (void)ok;
+            if ((!ok || *abort_flag) && last > 0) {
+                // Abort: this lane's last copy may still be landing in this CTA's
+                // shared memory.  Its completion is counted on the even CTA's
+                // stage barrier, so the even CTA waits (bounded) for that phase;
+                // the odd CTA cannot wait on a peer's barrier and lets a fixed,
+                // generous settle time pass instead.  Both then meet at the
+                // cluster barrier before either releases its memory.
+                if (even) wait_drain(smem_u32(&full[s]), ((last - 1) / kStages) & 1, tmo);
+                else settle_ns(kAbortSettleNs);
+            }
         }
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer (even CTA, whole warp)
@@ -1727,17 +1774,76 @@ dsnq_status check_consumer(const Consumer& c, int64_t K) {
     return DSNQ_OK;
 }
 
-template <int BN, bool SWAP, int STAGES, int NBUF, int EPI_WARPS, int AQ = 0>
+
+// ---- Kernel variant of a call, chosen on the host from (M, K) alone.
+// The variants and their shared-memory sizes per CTA (227 KB at most):
+//   decode (M <= 64, swap-AB, tokens as the MMA's N = 16 / 32 / 64);
+//   128 x 128 tiles (64 < M < 256; and M >= 256 when the CTA-pair kernel's
+//     scale slots do not fit, K > 4096), five operand stages while they fit
+//     beside the scale slots (K <= 4096), three beyond;
+//   CTA pair, 256 x 256 tiles (M >= 256, K <= 4096);
+//   decode on bf16 activations quantized (and normalized) in the prologue.
+enum Variant : int32_t {
+    kVarDecode16 = 1,
+    kVarDecode32 = 2,
+    kVarDecode64 = 3,
+    kVarTile128 = 4,
+    kVarTile128K = 5,          // three stages: room for the scale slots of long K
+    kVarPair = 6,
+    kVarDecodeQuant = 7,       // bf16 activations quantized in the prologue
+    kVarDecodeNormQuant = 8,   // ... after an RMSNorm
+};
+
+constexpr size_t kMaxSmem = 227 * 1024;
+
+size_t variant_smem(int v, int KB) {
+    switch (v) {
+        case kVarDecode16: return gemm::smem_bytes<16, true, 5, 16, 8>(KB);
+        case kVarDecode32: return gemm::smem_bytes<32, true, 5, 8, 8>(KB);
+        case kVarDecode64: return gemm::smem_bytes<64, true, 8, 8, 8>(KB);
+        case kVarTile128: return gemm::smem_bytes<128, false, 5, 4, 16>(KB);
+        case kVarTile128K: return gemm::smem_bytes<128, false, 3, 4, 16>(KB);
+        case kVarPair: return gemm::pair::smem_bytes(KB);
+        case kVarDecodeQuant: return gemm::smem_bytes<16, true, 8, 32, 8, 1>(KB);
+        case kVarDecodeNormQuant: return gemm::smem_bytes<16, true, 8, 32, 8, 2>(KB);
+    }
+    return 0;
+}
+
+// aq: 0 pre-quantized activations, 1 bf16 quantized in the kernel, 2 the
+// same after an RMSNorm.  UNSUPPORTED when no variant serves (M, K).
+dsnq_status plan_gemm(int64_t M, int64_t K, int aq, int* variant, size_t* smem) {
+    if (M < 1 || K < 128 || K % 128 != 0 || K > 8192 || M > 0x7fffffffLL) return DSNQ_ERR_UNSUPPORTED;
+    const int KB = static_cast<int>(K / 128);
+    int v;
+    if (aq) {
+        if (!bf16a_in_gemm(M, K)) return DSNQ_ERR_UNSUPPORTED;
+        v = aq == 2 ? kVarDecodeNormQuant : kVarDecodeQuant;
+    } else if (M <= 64) {
+        v = M <= 16 ? kVarDecode16 : M <= 32 ? kVarDecode32 : kVarDecode64;
+    } else if (M >= 256 && variant_smem(kVarPair, KB) <= kMaxSmem) {
+        v = kVarPair;
+    } else {
+        v = variant_smem(kVarTile128, KB) <= kMaxSmem ? kVarTile128 : kVarTile128K;
+    }
+    const size_t bytes = variant_smem(v, KB);
+    if (bytes > kMaxSmem) return DSNQ_ERR_UNSUPPORTED;
+    *variant = v;
+    *smem = bytes;
+    return DSNQ_OK;
+}
+
+template <int BN, bool SWAP, int STAGES, int NBUF, int EPI_WARPS, int AQ = 0, int MINB = 1>
 dsnq_status launch(gemm::Params& prm, const CUtensorMap& ma, const CUtensorMap& mw0, const CUtensorMap& mw1,
                    const CUtensorMap& mo0, const CUtensorMap& mo1, cudaStream_t stream) {
     using C = gemm::Cfg<BN, SWAP, STAGES, NBUF, EPI_WARPS, AQ>;
-    auto kern = gemm::block_scaled_gemm_kernel<BN, SWAP, STAGES, NBUF, EPI_WARPS, AQ>;
+    auto kern = gemm::block_scaled_gemm_kernel<BN, SWAP, STAGES, NBUF, EPI_WARPS, AQ, MINB>;
     const size_t smem = gemm::smem_bytes<BN, SWAP, STAGES, NBUF, EPI_WARPS, AQ>(prm.KB);
     if (smem > 227 * 1024) return DSNQ_ERR_UNSUPPORTED;
     if (!set_smem_attr(reinterpret_cast<const void*>(kern), smem)) return DSNQ_ERR_CUDA;
-    // Persistent: one CTA per SM (the shared-memory ring allows one), each
-    // walking the tile space with a stride of the grid size.
-    const int sms = device_sm_count();
+    // Persistent: MINB CTAs per SM (as many as the shared-memory ring and
+    // TMEM allow), each walking the tile space with a stride of the grid size.
+    const int sms = device_sm_count() * MINB;
     const int grid = prm.total_tiles < sms ? prm.total_tiles : (sms > 0 ? sms : prm.total_tiles);
     return launch_result(launch_kernel(kern, dim3(grid), dim3(C::kThreads), smem, stream, ma, mw0, mw1, mo0, mo1, prm));
 }
@@ -1827,12 +1933,17 @@ dsnq_status run_gemm(int64_t M, int64_t K, const void* a, int64_t lda, const flo
     if (st != DSNQ_OK) return st;
     if (c0.N == 0 && c1.N == 0) return DSNQ_OK;
 
-    // Decode batches (M <= 64): swap-AB, the tokens are the MMA's N.  From
-    // 256 rows on, 256 x 256 tiles on CTA pairs; in between 128x128 tiles
-    // with four TMEM partial buffers.
-    const bool swap = M <= 64;
-    const bool paired = !swap && M >= 256;
-    const int bn = swap ? (M <= 16 ? 16 : M <= 32 ? 32 : 64) : 128;
+    // The variant: decode batches (M <= 64) run swap-AB, the tokens being the
+    // MMA's N; from 256 rows on 256 x 256 tiles on CTA pairs; in between (and
+    // for long K) 128 x 128 tiles with four TMEM partial buffers.
+    int variant = 0;
+    size_t smem_plan = 0;
+    st = plan_gemm(M, K, aq ? (ns ? 2 : 1) : 0, &variant, &smem_plan);
+    if (st != DSNQ_OK) return st;
+    (void)smem_plan;
+    const bool swap = variant <= kVarDecode64 || variant >= kVarDecodeQuant;
+    const bool paired = variant == kVarPair;
+    const int bn = swap ? (variant == kVarDecode32 ? 32 : variant == kVarDecode64 ? 64 : 16) : 128;
     const int a_box = swap ? bn : gemm::kPRows;
     // The CTA-pair kernel loads weight rows in chunks of 64 (each CTA's share
     // of an N=128 MMA).
@@ -1908,20 +2019,24 @@ dsnq_status run_gemm(int64_t M, int64_t K, const void* a, int64_t lda, const flo
     prm.inject = g_inject.load();
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (aq)
-        return ns ? launch<16, true, 8, 32, 8, 2>(prm, ma, mw[0], mw[1], mo[0], mo[1], s)
-                  : launch<16, true, 8, 32, 8, 1>(prm, ma, mw[0], mw[1], mo[0], mo[1], s);
-    if (paired) return launch_pair(prm, ma, mw[0], mw[1], mo[0], mo[1], s);
-    switch (bn) {
-        // Decode: the MMA per K block is tiny, so the MMA <-> promotion round
-        // trip sets the pace; a TMEM ring as deep as TMEM allows (512 / BN
-        // buffers) lets the MMA run a whole tile ahead of the promotion.
-        case 16: return launch<16, true, 8, 32, 8>(prm, ma, mw[0], mw[1], mo[0], mo[1], s);
-        case 32: return launch<32, true, 8, 16, 8>(prm, ma, mw[0], mw[1], mo[0], mo[1], s);
-        case 64: return launch<64, true, 8, 8, 8>(prm, ma, mw[0], mw[1], mo[0], mo[1], s);
-        default:
-            if (KB <= 16) return launch<128, false, 5, 4, 16>(prm, ma, mw[0], mw[1], mo[0], mo[1], s);
-            return launch<128, false, 3, 4, 16>(prm, ma, mw[0], mw[1], mo[0], mo[1], s);
+    switch (variant) {
+        case kVarDecodeQuant: return launch<16, true, 8, 32, 8, 1>(prm, ma, mw[0], mw[1], mo[0], mo[1], s);
+        case kVarDecodeNormQuant: return launch<16, true, 8, 32, 8, 2>(prm, ma, mw[0], mw[1], mo[0], mo[1], s);
+        case kVarPair: return launch_pair(prm, ma, mw[0], mw[1], mo[0], mo[1], s);
+        // Decode: the kernel streams the weights.  Up to 32 tokens two CTAs
+        // share an SM (five stages, half of TMEM each), so that all 224
+        // weight tiles of the DSv4 dual problem stream at once on 152 SMs
+        // instead of 72 SMs taking a second tile after the others finish
+        // (M=1: 12.1 -> 10.8 us per call in a graph).  The MMA per K block is
+        // tiny, so the MMA <-> promotion round trip sets the pace within a
+        // CTA; its TMEM ring (256 / BN buffers) lets the MMA run most of a
+        // tile ahead of the promotion.  64 tokens keep one CTA per SM (two
+        // measured 4x slower).
+        case kVarDecode16: return launch<16, true, 5, 16, 8, 0, 2>(prm, ma, mw[0], mw[1], mo[0], mo[1], s);
+        case kVarDecode32: return launch<32, true, 5, 8, 8, 0, 2>(prm, ma, mw[0], mw[1], mo[0], mo[1], s);
+        case kVarDecode64: return launch<64, true, 8, 8, 8>(prm, ma, mw[0], mw[1], mo[0], mo[1], s);
+        case kVarTile128: return launch<128, false, 5, 4, 16>(prm, ma, mw[0], mw[1], mo[0], mo[1], s);
+        default: return launch<128, false, 3, 4, 16>(prm, ma, mw[0], mw[1], mo[0], mo[1], s);
     }
 }
 
@@ -1948,6 +2063,31 @@ extern "C" dsnq_status dsnq_block_scaled_fp8_gemm_dual(
     Consumer c0{N1, w1_fp8, ldw1, w1_scale, ld_w1scale, out1_bf16, ldo1};
     Consumer c1{N2, w2_fp8, ldw2, w2_scale, ld_w2scale, out2_bf16, ldo2};
     return run_gemm(M, K, a_fp8, lda, a_scale, a_scale_layout, ld_ascale, c0, c1, stream);
+}
+
+extern "C" dsnq_status dsnq_gemm_plan(int64_t M, int64_t K, int32_t* variant, int64_t* smem_bytes) {
+    if (M < 0 || K <= 0) return DSNQ_ERR_INVALID_ARG;
+    if (M == 0) {
+        if (variant) *variant = 0;
+        if (smem_bytes) *smem_bytes = 0;
+        return DSNQ_OK;
+    }
+    int v = 0;
+    size_t smem = 0;
+    const dsnq_status st = plan_gemm(M, K, 0, &v, &smem);
+    if (st != DSNQ_OK) return st;
+    if (variant) *variant = v;
+    if (smem_bytes) *smem_bytes = static_cast<int64_t>(smem);
+    return DSNQ_OK;
+}
+
+extern "C" dsnq_status dsnq_bf16a_workspace_bytes(int64_t M, int64_t K, int64_t* code_bytes, int64_t* scale_bytes) {
+    if (M < 0 || K <= 0) return DSNQ_ERR_INVALID_ARG;
+    if (K % 128 != 0 || K > 4096) return DSNQ_ERR_UNSUPPORTED;
+    const bool none = M == 0 || bf16a_in_gemm(M, K);
+    if (code_bytes) *code_bytes = none ? 0 : M * K;
+    if (scale_bytes) *scale_bytes = none ? 0 : M * (K / 128) * static_cast<int64_t>(sizeof(float));
+    return DSNQ_OK;
 }
 
 extern "C" dsnq_status dsnq_block_scaled_fp8_gemm_dual_bf16a(

@@ -46,25 +46,44 @@ struct GroupQuant {
     bool exact;             // reciprocal not finite: divide
 };
 
-__device__ __forceinline__ GroupQuant make_group_quant(float amax) {
-    GroupQuant gq;
-    // scale = RN(amax / 448) by the correction step of Markstein's division
-    // method: with y = RN(1/448), q0 = RN(amax * y) and the exact remainder
-    // amax - q0 * 448 (one FMA), RN(q0 + remainder * y) is the correctly
-    // rounded quotient for every amax >= 2^-96 (checked exhaustively over a
-    // binade, and across binades, in the test suite); below that, the division.
+// scale = RN(amax / 448) by the correction step of Markstein's division
+// method: with y = RN(1/448), q0 = RN(amax * y) and the exact remainder
+// amax - q0 * 448 (one FMA), RN(q0 + remainder * y) is the correctly rounded
+// quotient for every amax >= 2^-96 (checked exhaustively over a binade, and
+// across binades, in the test suite); below that, the division.
+__device__ __forceinline__ float group_scale(float amax) {
     constexpr float kRecip448 = 1.0f / kE4M3Max;
     const float q0 = __fmul_rn(amax, kRecip448);
-    gq.scale = fmaf(fmaf(-q0, kE4M3Max, amax), kRecip448, q0);
-    if (amax < 0x1p-96f) gq.scale = amax / kE4M3Max;
-    gq.exact = gq.scale > 0.f && gq.scale < 1.0e-36f;
-    const float y = (gq.scale > 0.f && !gq.exact) ? __fdividef(1.0f, gq.scale) : 0.f;
-    // y is within 2^-22 of 1/scale; each product below adds at most 2^-24,
-    // so x*ylo <= x/scale <= x*yhi (in magnitude order) with room to spare.
+    float scale = fmaf(fmaf(-q0, kE4M3Max, amax), kRecip448, q0);
+    if (amax < 0x1p-96f) scale = amax / kE4M3Max;
+    return scale;
+}
+
+// Groups whose scale is too small for a finite reciprocal take the division.
+__device__ __forceinline__ bool group_needs_division(float scale) { return scale > 0.f && scale < 1.0e-36f; }
+
+// The reciprocal the bracket scales (0 for an all-zero group and for groups
+// that take the division): within 2^-22 of 1/scale (fast divide, 2 ulp).
+__device__ __forceinline__ float group_recip(float scale) {
+    return (scale > 0.f && !group_needs_division(scale)) ? __fdividef(1.0f, scale) : 0.f;
+}
+
+// The bracket of a group from its scale and reciprocal.  Each product below
+// adds at most 2^-24 to the reciprocal's 2^-22, so x*ylo <= x/scale <= x*yhi
+// (in magnitude order) with room to spare.
+__device__ __forceinline__ GroupQuant group_quant_from(float scale, float y) {
+    GroupQuant gq;
+    gq.scale = scale;
+    gq.exact = group_needs_division(scale);
     const float lo = y * (1.0f - 0x1p-20f), hi = y * (1.0f + 0x1p-20f);
     gq.ylo = make_float2(lo, lo);
     gq.yhi = make_float2(hi, hi);
     return gq;
+}
+
+__device__ __forceinline__ GroupQuant make_group_quant(float amax) {
+    const float scale = group_scale(amax);
+    return group_quant_from(scale, group_recip(scale));
 }
 
 // Codes of eight values by the bracket (E4M3 rounding is monotone, so when

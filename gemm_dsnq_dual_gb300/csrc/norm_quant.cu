@@ -375,38 +375,50 @@ warp_row_kernel(const RowArgs a) {
 }
 
 // ---------------------------------------------------------------------------
-// Fused warp-per-row kernel for rows whose q and kv parts are whole warp
-// slots (Kq and Kkv multiples of 256: QS slots of q, KS of kv; DSv4: 6 + 2).
+// Fused warp-per-row kernel for the DSv4 row: Kq = 1536 (6 slots of 256
+// columns, one 128-column group per half-warp and slot) and Kkv = 512 (2
+// slots).  Lane l holds chunks l, l+32, ... of the row (16 bytes each).
 //   * each slot's role is known at compile time (no per-chunk predicates);
 //   * the next row of the warp is loaded into registers as soon as the
 //     current one is unpacked, and the row after it is prefetched into L2;
-//   * 4 CTAs of 4 warps per SM (128 registers): the kernel is bound by its
-//     instruction latency, so warps in flight matter more than ILP per warp;
-//   * the row is processed in phases over all slots (sums of squares, norm,
-//     group amax, scales, codes) so that the independent chains overlap;
+//   * the work that is the same for a whole warp is done once, by the lanes
+//     it concerns, and handed to the others by shuffles:
+//       - the two sums of squares are reduced by a reduce-scatter (lanes
+//         0-15 end with the q sum, 16-31 with the kv sum), each half takes
+//         its 1/sqrt(mean + eps) in one IEEE chain, two shuffles broadcast;
+//       - the twelve group maxima are reduced by a reduce-scatter over the
+//         six q slots (lanes with lane bit 3 clear keep slots 0-2, set 3-5),
+//         so that lane 16h + 8b + i (i < 3) holds group 2(3b + i) + h: that
+//         lane alone forms the group's scale and reciprocal, stores the
+//         scale, and the other lanes fetch both by shuffle;
 //   * the quantize step uses bracket reciprocals scaled once per group and
-//     takes the exactness decision for the whole row with one warp vote.
+//     takes the exactness decision for three slots with one warp vote.
 // ---------------------------------------------------------------------------
 constexpr int kFusedCtasPerSM = 4;  // register budget: 128 per thread
 
 template <int QS, int KS>
 __global__ void __launch_bounds__(kRowWarps * 32, kFusedCtasPerSM)
 warp_row_fused_kernel(const RowArgs a) {
+    static_assert(QS == 6 && KS == 2, "the lane roles below are laid out for the DSv4 row");
     grid_dependency_wait();      // inputs are read only once the previous kernel's writes are visible
     allow_dependent_launch();
     constexpr int CPT = QS + KS;
+    constexpr unsigned kAll = 0xffffffffu;
     extern __shared__ float gamma_s[];          // [(QS + KS) * 256] fp32: gamma_q then gamma_kv
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     constexpr int kq = QS * 256, width = CPT * 256;
+    const bool q_half = lane < 16;              // reduce-scatter roles
+    const bool hi8 = (lane & 8) != 0;
+    const int gi = lane & 7;                    // group slot this lane forms (when < 3)
+    const int h = lane >> 4;                    // half-warp: group 2j + h in slot j
 
     auto load_row = [&](int64_t m, uint4 (&raw)[CPT]) {
+        const __nv_bfloat16* qrow = a.q + m * a.ldq + lane * kChunk;
+        const __nv_bfloat16* kvrow = a.kv + m * a.ldkv + lane * kChunk;
 #pragma unroll
-        for (int j = 0; j < CPT; ++j) {
-            const __nv_bfloat16* src = j < QS ? a.q + m * a.ldq + (j * 32 + lane) * kChunk
-                                              : a.kv + m * a.ldkv + ((j - QS) * 32 + lane) * kChunk;
-            raw[j] = __ldg(reinterpret_cast<const uint4*>(src));
-        }
+        for (int j = 0; j < CPT; ++j)
+            raw[j] = __ldg(reinterpret_cast<const uint4*>(j < QS ? qrow + j * 256 : kvrow + (j - QS) * 256));
     };
 
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kRowWarps;
@@ -429,12 +441,16 @@ warp_row_fused_kernel(const RowArgs a) {
         asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
     };
     if (m + stride < a.M) prefetch_l2(m + stride);
+    const float kdiv = q_half ? a.kq_f : a.kkv_f;
     for (; m < a.M; m += stride) {
         if (m + 2 * stride < a.M) prefetch_l2(m + 2 * stride);
         float2 x[CPT][4];
 #pragma unroll
         for (int j = 0; j < CPT; ++j) unpack8(cur[j], x[j]);
         if (m + stride < a.M) load_row(m + stride, cur);   // next row (in L2 by now), in flight meanwhile
+
+        // Sums of squares, then the reduce-scatter: lanes 0-15 finish the q
+        // sum, lanes 16-31 the kv sum, each over the 32 lanes' partials.
         float2 sq[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
         float2 skv[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
@@ -445,11 +461,14 @@ warp_row_fused_kernel(const RowArgs a) {
                 else skv[i & 1] = fma2(x[j][i], x[j][i], skv[i & 1]);
             }
         }
-        const float ssq_q = warp_sum((sq[0].x + sq[1].x) + (sq[0].y + sq[1].y));
-        const float ssq_kv = warp_sum((skv[0].x + skv[1].x) + (skv[0].y + skv[1].y));
-        // Correctly rounded sqrt and divide (not the approximate rsqrt).
-        const float rq = 1.0f / sqrtf(ssq_q / a.kq_f + a.eps);
-        const float rkv = 1.0f / sqrtf(ssq_kv / a.kkv_f + a.eps);
+        const float pq = (sq[0].x + sq[1].x) + (sq[0].y + sq[1].y);
+        const float pkv = (skv[0].x + skv[1].x) + (skv[0].y + skv[1].y);
+        float ssq = (q_half ? pq : pkv) + __shfl_xor_sync(kAll, q_half ? pkv : pq, 16);
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) ssq += __shfl_xor_sync(kAll, ssq, o);
+        // Correctly rounded division and sqrt (not the approximate rsqrt).
+        const float rr = 1.0f / sqrtf(ssq / kdiv + a.eps);
+        const float rq = __shfl_sync(kAll, rr, 0), rkv = __shfl_sync(kAll, rr, 16);
 
         // Normalize; kv goes straight out.
 #pragma unroll
@@ -466,19 +485,33 @@ warp_row_fused_kernel(const RowArgs a) {
             if (j >= QS) *reinterpret_cast<uint4*>(a.kv_out + m * a.ldkv_out + col) = pack8_bf16(x[j]);
         }
 
-        // Group amax (one 128-column group per half-warp and q slot).
+        // Group maxima: this lane's eight values per q slot, then the
+        // reduce-scatter across the half-warp (slots 0-2 stay with lanes whose
+        // bit 3 is clear, 3-5 with the others), then a butterfly on three.
         float am[QS];
 #pragma unroll
         for (int j = 0; j < QS; ++j)
             am[j] = fmaxf(fmaxf(fmaxf(fabsf(x[j][0].x), fabsf(x[j][0].y)), fmaxf(fabsf(x[j][1].x), fabsf(x[j][1].y))),
                           fmaxf(fmaxf(fabsf(x[j][2].x), fabsf(x[j][2].y)), fmaxf(fabsf(x[j][3].x), fabsf(x[j][3].y))));
+        float kmax[3];
 #pragma unroll
-        for (int o = 8; o > 0; o >>= 1) {
+        for (int i = 0; i < 3; ++i)
+            kmax[i] = fmaxf(hi8 ? am[3 + i] : am[i], __shfl_xor_sync(kAll, hi8 ? am[i] : am[3 + i], 8));
 #pragma unroll
-            for (int j = 0; j < QS; ++j) am[j] = fmaxf(am[j], __shfl_xor_sync(0xffffffffu, am[j], o));
+        for (int o = 4; o > 0; o >>= 1) {
+#pragma unroll
+            for (int i = 0; i < 3; ++i) kmax[i] = fmaxf(kmax[i], __shfl_xor_sync(kAll, kmax[i], o));
+        }
+        // Lane 16h + 8b + i (i < 3) forms group 2(3b + i) + h; the other lanes
+        // compute a copy they discard.
+        const float own_scale = group_scale(gi == 0 ? kmax[0] : gi == 1 ? kmax[1] : kmax[2]);
+        const float own_y = group_recip(own_scale);
+        if (gi < 3) {
+            const int g = 2 * (3 * (hi8 ? 1 : 0) + gi) + h;
+            a.scale[m * a.scale_row_stride + g * a.scale_group_stride] = own_scale;
         }
 
-        // Scales and codes, three q slots at a time (fewer live registers).
+        // Codes, three q slots at a time (fewer live registers).
         constexpr int kGrp = 3;
         static_assert(QS % kGrp == 0, "q slots in groups of three");
 #pragma unroll
@@ -488,12 +521,14 @@ warp_row_fused_kernel(const RowArgs a) {
             bool ok_all = true;
 #pragma unroll
             for (int u = 0; u < kGrp; ++u) {
-                gq[u] = make_group_quant(am[j0 + u]);
+                const int j = j0 + u;                       // slot j: group 2j + h, formed by lane 16h + 8(j/3) + j%3
+                const int src = (lane & 16) | ((j / 3) << 3) | (j % 3);
+                gq[u] = group_quant_from(__shfl_sync(kAll, own_scale, src), __shfl_sync(kAll, own_y, src));
                 bool ok;
-                codes[u] = quant8_bracket(x[j0 + u], gq[u], ok);
+                codes[u] = quant8_bracket(x[j], gq[u], ok);
                 ok_all = ok_all && ok;
             }
-            if (!__all_sync(0xffffffffu, ok_all)) {
+            if (!__all_sync(kAll, ok_all)) {
 #pragma unroll
                 for (int u = 0; u < kGrp; ++u) {
                     bool ok;
@@ -502,15 +537,10 @@ warp_row_fused_kernel(const RowArgs a) {
                     codes[u] = quant8_divide(x[j0 + u], gq[u].scale);
                 }
             }
+            uint8_t* crow = a.q_fp8 + m * a.ldq_out + lane * kChunk;
 #pragma unroll
-            for (int u = 0; u < kGrp; ++u) {
-                const int col = (j0 + u) * 256 + lane * kChunk;
-                *reinterpret_cast<uint2*>(a.q_fp8 + m * a.ldq_out + col) = codes[u];
-                if ((lane & 15) == 0)
-                    a.scale[m * a.scale_row_stride + (col / 128) * a.scale_group_stride] = gq[u].scale;
-            }
+            for (int u = 0; u < kGrp; ++u) *reinterpret_cast<uint2*>(crow + (j0 + u) * 256) = codes[u];
         }
-
     }
 }
 

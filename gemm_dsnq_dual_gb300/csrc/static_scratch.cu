@@ -60,7 +60,10 @@ extern "C" dsnq_status dsnq_block_scaled_fp8_gemm_dual_bf16a_static(
     const float* w1_scale, int64_t ld_w1scale, void* out1_bf16, int64_t ldo1, int64_t N2, const void* w2_fp8,
     int64_t ldw2, const float* w2_scale, int64_t ld_w2scale, void* out2_bf16, int64_t ldo2, void* stream) {
     using namespace dsnq;
-    if (M < 0 || K <= 0) return DSNQ_ERR_INVALID_ARG;
+    // The same size checks as the workspace entry, before the early returns,
+    // so both report the same status for the same bad input.
+    if (M < 0 || K <= 0 || N1 < 0 || N2 < 0) return DSNQ_ERR_INVALID_ARG;
+    if (K % 128 != 0) return DSNQ_ERR_UNSUPPORTED;
     if (M > kScratchRows || K > kScratchK) return DSNQ_ERR_UNSUPPORTED;
     if (M == 0) return DSNQ_OK;
     ScratchPtrs ws{};

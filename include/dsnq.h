@@ -225,8 +225,10 @@ DSNQ_API dsnq_status dsnq_quantize_weight_block128(
  *                ldw >= K, ldw % 16 == 0, 16-byte aligned.
  *   w_scale, ld_wscale : fp32 [ceil(N/128), K/128], ld_wscale >= K/128.
  *   out_bf16, ldo : bf16 [M, N], ldo >= N, ldo % 8 == 0, 16-byte aligned.
- * K must be a multiple of 128 and at most 8192 (DSNQ_ERR_UNSUPPORTED otherwise) and N a
- * multiple of 16.  The output must not overlap the inputs.
+ * K must be a multiple of 128 and at most 8192 (DSNQ_ERR_UNSUPPORTED otherwise,
+ * before anything is enqueued) and N a multiple of 16; every M >= 1 and every
+ * such K is served (dsnq_gemm_plan names the kernel variant a call takes).
+ * The output must not overlap the inputs.
  */
 DSNQ_API dsnq_status dsnq_block_scaled_fp8_gemm(
     int64_t M, int64_t N, int64_t K,
@@ -254,6 +256,36 @@ DSNQ_API dsnq_status dsnq_block_scaled_fp8_gemm_dual(
     int64_t N2, const void* w2_fp8, int64_t ldw2, const float* w2_scale, int64_t ld_w2scale,
     void* out2_bf16, int64_t ldo2,
     void* stream);
+
+/*
+ * Host-only query (no CUDA call): the kernel variant dsnq_block_scaled_fp8_gemm
+ * and dsnq_block_scaled_fp8_gemm_dual launch for M activation rows and
+ * reduction length K, and its dynamic shared memory per CTA in bytes.  No
+ * counterpart in the published method: it describes this implementation.
+ *   variant : 1 / 2 / 3  decode, M <= 16 / 32 / 64: swap-AB, the weights fill
+ *                        the MMA's 128 rows and the tokens are its N;
+ *             4          128 x 128 tiles, five-stage operand ring (64 < M < 256,
+ *                        K <= 4096);
+ *             5          128 x 128 tiles, three-stage ring (M > 64, K > 4096:
+ *                        the ring gives way to the scale slots of long K);
+ *             6          256 x 256 tiles on CTA pairs (M >= 256, K <= 4096).
+ *   M == 0 reports variant 0 and 0 bytes (nothing would be launched).
+ * DSNQ_ERR_UNSUPPORTED when no variant serves (M, K): K not a multiple of
+ * 128 or K > 8192.  DSNQ_ERR_INVALID_ARG for M < 0 or K <= 0.  Either output
+ * pointer may be NULL.
+ */
+DSNQ_API dsnq_status dsnq_gemm_plan(int64_t M, int64_t K, int32_t* variant, int64_t* smem_bytes);
+
+/*
+ * Host-only query: the workspace dsnq_block_scaled_fp8_gemm_dual_bf16a needs
+ * for M rows of K bf16 activations, as the byte sizes of its two buffers
+ * (codes, scales); both 0 when the call quantizes inside the GEMM and reads
+ * no workspace.  No counterpart in the published method.
+ * DSNQ_ERR_UNSUPPORTED for K not a multiple of 128 or K > 4096;
+ * DSNQ_ERR_INVALID_ARG for M < 0 or K <= 0.  Either output may be NULL.
+ */
+DSNQ_API dsnq_status dsnq_bf16a_workspace_bytes(int64_t M, int64_t K, int64_t* code_bytes,
+                                                int64_t* scale_bytes);
 
 /*
  * The dual GEMM for callers without a pre-quantized pair: bf16 activations
@@ -292,10 +324,13 @@ DSNQ_API dsnq_status dsnq_block_scaled_fp8_gemm_dual_bf16a(
  * quantized pair goes to a device array inside the library (2048 x 2048
  * codes and their scales), so the call allocates nothing.  No counterpart in
  * the published method: an interface variant of this implementation.
- * M <= 2048 and K <= 2048 (DSNQ_ERR_UNSUPPORTED otherwise); other arguments
- * and rules as in dsnq_block_scaled_fp8_gemm_dual_bf16a.  Calls that use the
- * array (those outside the one-launch case) share it: on one device they must
- * be ordered, e.g. issued to one stream.
+ * M <= 2048 and K <= 2048 with K a multiple of 128 (DSNQ_ERR_UNSUPPORTED
+ * otherwise); other arguments and rules as in
+ * dsnq_block_scaled_fp8_gemm_dual_bf16a.  Calls that use the array (those
+ * outside the one-launch case) share it: on one device they must be ordered,
+ * e.g. issued to one stream, since calls that overlap on the GPU race on it.
+ * The first call on a device looks the array's address up (which may load
+ * the library's device code); make that first call before any stream capture.
  */
 DSNQ_API dsnq_status dsnq_block_scaled_fp8_gemm_dual_bf16a_static(
     int64_t M, int64_t K,

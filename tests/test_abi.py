@@ -183,6 +183,14 @@ def test_static_scratch_gemm_argument_checks(lib):
     assert call(M=-1) == INVALID
     assert call(M=2049) == UNSUPPORTED                     # beyond the library's scratch
     assert call(K=2176) == UNSUPPORTED
+    assert call(K=1000) == UNSUPPORTED                     # K % 128, fits the scratch
+    # Same status as the workspace entry for the same bad input, whatever M is.
+    g = lib.dsnq_block_scaled_fp8_gemm_dual_bf16a
+    for M in (0, 4, 4096):
+        st = f(M, 1536, A, 1536, -1, A, 1536, A, 12, A, 512, 256, A, 1536, A, 12, A, 256, None)
+        assert st == INVALID, M
+        assert g(M, 1536, A, 1536, -1, A, 1536, A, 12, A, 512, 256, A, 1536, A, 12, A, 256, None, None,
+                 None) == INVALID, M
 
 
 def test_fused_norm_quant_gemm_argument_checks(lib):
@@ -206,6 +214,48 @@ def test_fused_norm_quant_gemm_argument_checks(lib):
     assert call(qf=A + 8, qs=A) == MISALIGNED
     assert call(N1=520) == UNSUPPORTED                     # N % 16
     assert call(M=100) == INVALID                          # q_fp8 / q_scale needed above a few rows
+
+
+def test_gemm_plan_serves_every_k(lib):
+    """Host-only plan of the GEMM: every M >= 1 and every K that is a
+    multiple of 128 up to 8192 has a kernel variant whose shared memory fits
+    one SM (227 KB); other K are refused before anything is launched."""
+    v, b = C.c_int32(), C.c_int64()
+    seen = set()
+    for M in (1, 16, 17, 32, 33, 64, 65, 128, 255, 256, 300, 8192, 32768):
+        for K in range(128, 8192 + 1, 128):
+            assert lib.dsnq_gemm_plan(M, K, C.byref(v), C.byref(b)) == OK, (M, K)
+            assert 0 < b.value <= 227 * 1024, (M, K, b.value)
+            seen.add(v.value)
+            if M <= 16:
+                assert v.value == 1
+            elif M <= 32:
+                assert v.value == 2
+            elif M <= 64:
+                assert v.value == 3
+            elif M < 256:
+                assert v.value == (4 if K <= 4096 else 5), (M, K, v.value)
+            else:
+                assert v.value == (6 if K <= 4096 else 5), (M, K, v.value)
+        assert lib.dsnq_gemm_plan(M, 8320, C.byref(v), C.byref(b)) == UNSUPPORTED
+        assert lib.dsnq_gemm_plan(M, 1000, C.byref(v), C.byref(b)) == UNSUPPORTED
+    assert seen == {1, 2, 3, 4, 5, 6}
+    assert lib.dsnq_gemm_plan(0, 1536, C.byref(v), C.byref(b)) == OK and v.value == 0
+    assert lib.dsnq_gemm_plan(-1, 1536, None, None) == INVALID
+    # The calls themselves refuse K > 8192 on the host (no CUDA call is made here).
+    assert gemm(lib, M=300, K=8320, lda=8320, ldw=8320, ldsw=65) == UNSUPPORTED
+
+
+def test_bf16a_workspace_query(lib):
+    c, s = C.c_int64(), C.c_int64()
+    assert lib.dsnq_bf16a_workspace_bytes(1, 1536, C.byref(c), C.byref(s)) == OK
+    assert (c.value, s.value) == (0, 0)                   # quantized inside the GEMM
+    assert lib.dsnq_bf16a_workspace_bytes(100, 1536, C.byref(c), C.byref(s)) == OK
+    assert (c.value, s.value) == (100 * 1536, 100 * 12 * 4)
+    assert lib.dsnq_bf16a_workspace_bytes(0, 1536, C.byref(c), C.byref(s)) == OK
+    assert (c.value, s.value) == (0, 0)
+    assert lib.dsnq_bf16a_workspace_bytes(4, 8192, None, None) == UNSUPPORTED
+    assert lib.dsnq_bf16a_workspace_bytes(-1, 1536, None, None) == INVALID
 
 
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):

@@ -66,6 +66,26 @@ def test_gemm_shapes(M, N, K, layout):
     check_gemm(out, a.numpy(), sa.numpy(), wc, ws)
 
 
+# Long K: each kernel variant at the largest K it serves, and the variant
+# that takes over beyond it (the plan is checked too, so every variant of
+# dsnq_gemm_plan is reached here).
+LONG_K = [(1, 256, 8192, 1), (20, 256, 8192, 2), (40, 384, 8192, 3), (100, 256, 4096, 4),
+          (100, 256, 4224, 5), (200, 256, 8192, 5), (300, 256, 4096, 6), (300, 256, 4224, 5),
+          (520, 384, 8192, 5)]
+
+
+@pytest.mark.parametrize("M,N,K,variant", LONG_K)
+@pytest.mark.parametrize("layout", [dsnq.ROW_MAJOR, dsnq.COL_MAJOR])
+def test_gemm_long_k_every_variant(M, N, K, variant, layout):
+    assert dsnq.gemm_plan(M, K)[0] == variant
+    a, sa = inputs.random_codes_and_scales(M, K, seed=M + K)
+    wc, ws = quantized_weight(N, K, seed=N + K + 1)
+    out = dsnq.block_scaled_fp8_gemm(a.cuda(), scales_in_layout(sa, layout, pad=1),
+                                     torch.from_numpy(wc).cuda(), torch.from_numpy(ws).cuda())
+    torch.cuda.synchronize()
+    check_gemm(out, a.numpy(), sa.numpy(), wc, ws)
+
+
 def test_output_guard_and_padded_strides():
     M, N, K = 70, 384, 512
     a, sa = inputs.random_codes_and_scales(M, K, seed=1)

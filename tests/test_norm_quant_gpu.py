@@ -213,6 +213,31 @@ def test_baseline_group_quant_bf16(layout):
     assert_codes_close(u8(codes), wc)
 
 
+@pytest.mark.parametrize("M", [8192, 32768])
+def test_baseline_large_m_column_major(M):
+    """The unfused three-launch sequence at the sizes the bench times it
+    (the warp-per-row kernels in their norm-only and quant-only modes):
+    dual RMSNorm to bf16, then the per-1x128 quant of the bf16 q, checked
+    against the oracle on every row (M=8192) or on a seeded sample plus the
+    first and last rows (M=32768)."""
+    lat = inputs.prefill_batch(M, seed=13) if M == 8192 else inputs.long_context_batch(M, seed=14)
+    q, kv = lat.q.cuda(), lat.kv.cuda()
+    qo, kvo = dsnq.dual_rmsnorm_bf16(q, kv, lat.gamma_q.cuda(), lat.gamma_kv.cuda(), lat.eps)
+    codes, scale = dsnq.group_quant_bf16(qo, scale_layout="col")
+    torch.cuda.synchronize()
+    rows = np.arange(M) if M == 8192 else np.array(sorted(
+        {0, 1, M - 2, M - 1} | set(np.random.default_rng(2).choice(M, 2048, replace=False).tolist())))
+    b = [inputs.bits(t[rows]) for t in (lat.q, lat.kv)]
+    wq, wkv = oracle.dual_rmsnorm_bf16(b[0], b[1], inputs.bits(lat.gamma_q), inputs.bits(lat.gamma_kv), lat.eps)
+    idx = torch.from_numpy(rows).cuda()
+    assert_bf16_close(u16(qo[idx]), wq)
+    assert_bf16_close(u16(kvo[idx]), wkv)
+    # The quant step is checked on the kernel's own bf16 q (its input).
+    wc, ws = oracle.group_quant_bf16(u16(qo[idx]))
+    assert_scales_close(scale[idx].cpu().numpy(), ws)
+    assert_codes_close(u8(codes[idx]), wc)
+
+
 def test_weight_block_quantizer():
     w = inputs.weight(4096 + 64, 1536, seed=9)          # ragged last block of 64 rows
     codes, sw = dsnq.quantize_weight_block128(w.cuda())

@@ -311,3 +311,50 @@ def test_single_latent_is_the_q_part_of_the_fused_op():
     ones = oracle.f64_to_bf16_bits(np.ones(256))
     c, s = oracle.rmsnorm_group_quant(const, ones, 0.0)
     assert np.all(c == 0x7E) and np.allclose(s, np.float32(1.0) / np.float32(448.0))
+
+
+def _plain_fp64_quotient_codes(q_bits, kv_bits, gq_bits, gkv_bits, eps, group=128):
+    """The quant step by its plain definition, all in fp64: x_hat from the
+    fp64 RMSNorm (not rounded to fp32), amax of x_hat, the scale stored as
+    fp32(amax / 448), and code = e4m3(x_hat / scale) with the quotient left in
+    fp64.  Written here from the definition, independently of the oracle's
+    fp32-quotient reading."""
+    eps = float(np.float32(eps))
+    x = oracle.bf16_bits_to_f64(q_bits)
+    ms = np.mean(x * x, axis=1, keepdims=True)
+    xhat = x / np.sqrt(ms + eps) * oracle.bf16_bits_to_f64(gq_bits)
+    M, K = xhat.shape
+    g = xhat.reshape(M, K // group, group)
+    s = (np.max(np.abs(g), axis=-1) / 448.0).astype(np.float32).astype(np.float64)[..., None]
+    quot = np.where(s > 0, g / np.where(s > 0, s, 1.0), g * 0.0)
+    return oracle.e4m3_encode(quot).reshape(M, K)
+
+
+@pytest.mark.parametrize("workload", ["decode", "prefill", "long_context"])
+def test_fp32_quotient_reading_stays_within_tolerance_of_the_plain_definition(workload):
+    """The oracle takes the quantize decision on the fp32 quotient (the
+    pages' "reads the fp32 accumulator").  Against the same step taken
+    entirely in fp64 (the plain definition, a different but well-defined
+    code), its codes are within one E4M3 step and at least 99.9% identical
+    on the workloads' inputs: the stated tolerance holds against the plain
+    definition too, not only against the reading."""
+    from parity import CODE_EXACT_MIN, code_ordinal
+    if workload == "decode":
+        lat = inputs.decode_batch(64, seed=1)
+        rows = slice(None)
+    elif workload == "prefill":
+        lat = inputs.prefill_batch(8192, seed=2)
+        rows = np.random.default_rng(5).choice(8192, 2048, replace=False)
+    else:
+        lat = inputs.long_context_batch(32768, seed=4)
+        M = 32768
+        edge = {0, M - 1} | set(range(0, M, 97)) | set(range(0, M, 89))
+        rows = np.array(sorted(edge | set(np.random.default_rng(6).choice(M, 1024, replace=False).tolist())))
+    b = [inputs.bits(t.contiguous()) for t in (lat.q, lat.kv)]
+    qb, kvb = b[0][rows], b[1][rows]
+    gq, gkv = inputs.bits(lat.gamma_q), inputs.bits(lat.gamma_kv)
+    codes, _, _ = oracle.fused_dual_rmsnorm_group_quant(qb, kvb, gq, gkv, lat.eps)
+    plain = _plain_fp64_quotient_codes(qb, kvb, gq, gkv, lat.eps)
+    d = np.abs(code_ordinal(codes) - code_ordinal(plain))
+    assert d.max() <= 1
+    assert (d == 0).mean() >= CODE_EXACT_MIN
