@@ -55,13 +55,23 @@ NQ_BYTES_PER_CALL = 2 * (KQ + KKV)                                      # gammas
 UNFUSED_BYTES_PER_ROW = (4096 + 4096) + 2 * (3072 + 1584)               # 17504
 
 
+def step_config(M: int, world: int) -> dict:
+    """The workload one step processes (the same for both arms)."""
+    return {"workload": f"full path: fused dual RMSNorm + per-1x128 FP8 quant of q[{M},1536]/kv[{M},512] "
+                        f"-> dual block-scaled FP8 GEMM (wq_b N=24576 + indexer wq_b N=4096, K=1536)",
+            "M": M, "Kq": KQ, "Kkv": KKV, "N": [N_ATTN, N_IDX], "scale_layout": "column-major",
+            "l2": "flushed before every timed step (256 MiB write + 256 MiB read)",
+            "parallelism": f"dp{world} (independent token batches, no collective)"}
+
+
 def gemm_flops(M: int) -> float:
     return 2.0 * M * (N_ATTN + N_IDX) * KQ
 
 
-def captured_traffic(key: str):
-    """DRAM bytes per launch (read + write) from the committed ncu summary, or
-    None when the kernel's source has changed since the capture."""
+def captured_traffic(key: str, field: str = "dram_bytes_per_launch"):
+    """DRAM bytes per launch (read + write), or another `field` of the record,
+    from the committed ncu summary; None when the kernel's source has changed
+    since the capture."""
     import hashlib
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
@@ -72,7 +82,7 @@ def captured_traffic(key: str):
     src = os.path.join(ROOT, "gemm_dsnq_dual_gb300", "csrc", rec["source"])
     if not os.path.exists(src) or hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] != rec["source_sha256_16"]:
         return None
-    return rec["dram_bytes_per_launch"]
+    return rec.get(field)
 
 
 def load_peaks():
@@ -224,7 +234,7 @@ def run_ours(args, rank, world):
     # ---- side measurements (rank 0 only; not part of the timed region)
     extra = {}
     if rank == 0:
-        extra = side_measurements(torch, dsnq, inputs, dev, flush, hbm_gbs, args)
+        extra = side_measurements(torch, dsnq, inputs, dev, flush, hbm_gbs, args, fp8_peak)
         extra["e2e"] = e2e_measurement(torch, dsnq, lat, dev, (wa, swa, wi, swi), args, M)
     if rank != 0:
         return
@@ -246,11 +256,7 @@ def run_ours(args, rank, world):
         "vs_baseline": None,
         "dtype": "e4m3xe4m3->f32 (GEMM); bf16->f32->e4m3/bf16 (norm+quant)",
         "data": "synthetic",
-        "config": {"workload": f"full path: fused dual RMSNorm + per-1x128 FP8 quant of q[{M},1536]/kv[{M},512] "
-                               f"-> dual block-scaled FP8 GEMM (wq_b N=24576 + indexer wq_b N=4096, K=1536)",
-                   "M": M, "Kq": KQ, "Kkv": KKV, "N": [N_ATTN, N_IDX], "scale_layout": "column-major",
-                   "l2": "flushed before every timed step (256 MiB write + 256 MiB read)",
-                   "parallelism": f"dp{world} (independent token batches, no collective)"},
+        "config": step_config(M, world),
         "gpu_launches": 2 * K,
         "kernels": {
             "norm_quant_us": round(nq_avg * 1e3, 3),
@@ -262,6 +268,7 @@ def run_ours(args, rank, world):
                      "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
                      "frac": round(gemm_tflops / fp8_peak, 4),
                      "traffic": captured_traffic(f"gemm_dual_M{M}"),
+                     "tensor_pipe_active_pct": captured_traffic(f"gemm_dual_M{M}", "tensor_pipe_active_pct"),
                      "algorithmic_bytes": int(M * (KQ + 4 * KQ // 128) + (N_ATTN + N_IDX) * KQ
                                               + 2 * M * (N_ATTN + N_IDX)),
                      "kernel": ("pair_gemm_kernel" if M >= 256 else "block_scaled_gemm_kernel") + " (one launch, both consumers)",
@@ -277,7 +284,38 @@ def run_ours(args, rank, world):
     line.update(extra)
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_rows)
+    line["headline"] = headline(line)     # last, so a tail of the line keeps it
     print(json.dumps(line), flush=True)
+
+
+def headline(line: dict) -> dict:
+    """The figures the metric is quoted on, compactly: norm+quant us at M=1
+    and fraction of HBM per M, the decode step, and the GEMM's TFLOP/s and
+    fraction of the FP8 peak at the full-path and long-context sizes."""
+    h = {"gemm_dual_M8192_tflops": line["roofline"]["achieved"], "gemm_dual_M8192_frac_fp8": line["roofline"]["frac"]}
+    if "norm_quant_us_at_M1" in line:
+        h["norm_quant_us_at_M1"] = line["norm_quant_us_at_M1"]
+    sw = line.get("norm_quant_sweep", {})
+    h["norm_quant_graph_frac_hbm"] = {m: v.get("fused_graph_frac_hbm") for m, v in sw.items() if isinstance(v, dict)}
+    h["norm_quant_speedup_vs_unfused"] = {m: v.get("speedup_vs_unfused") for m, v in sw.items() if isinstance(v, dict)}
+    h["norm_quant_step_frac_hbm_M8192"] = line["roofline_norm_quant"]["frac"]
+    if "decode_step_us_at_M1" in line:
+        h["decode_step_us_at_M1"] = line["decode_step_us_at_M1"].get("overlap")
+    gs = line.get("gemm_sweep", {})
+    if "1" in gs:
+        h["gemm_dual_M1_graph_us"] = gs["1"].get("graph_us")
+        h["gemm_dual_M1_graph_frac_hbm"] = gs["1"].get("graph_frac_hbm")
+    if "1024" in gs:
+        h["gemm_dual_M1024_tflops"] = gs["1024"].get("tflops")
+    if "32768_long_context_attn" in gs:
+        h["gemm_attn_M32768_tflops"] = gs["32768_long_context_attn"]["tflops"]
+        h["gemm_attn_M32768_frac_fp8"] = gs["32768_long_context_attn"]["frac_fp8"]
+    ds = line.get("decode_sweep", {})
+    h["norm_quant_decode_us"] = {m: [v["row_us"], v["col_us"]] for m, v in ds.items() if isinstance(v, dict)}
+    cb = line.get("cpu_baseline")
+    if cb:
+        h["cpu_oracle_tflops"] = {"cores": cb["cores"], "all": cb["value"], "one_thread": cb["single_thread"]["value"]}
+    return h
 
 
 def timed_graph_calls(torch, stream, fn_list, flush, reps=20):
@@ -307,7 +345,7 @@ def timed_graph_calls(torch, stream, fn_list, flush, reps=20):
     return statistics.median(times[2:])
 
 
-def side_measurements(torch, dsnq, inputs, dev, flush, hbm_gbs, args):
+def side_measurements(torch, dsnq, inputs, dev, flush, hbm_gbs, args, fp8_peak):
     stream = torch.cuda.current_stream()
     out = {}
     # -- M=1 decode latency: 100 calls, each on its own cold row of a split-view buffer
@@ -328,7 +366,8 @@ def side_measurements(torch, dsnq, inputs, dev, flush, hbm_gbs, args):
     out["norm_quant_us_at_M1_note"] = ("per call, CUDA graph of 100 calls on 100 distinct cold rows, L2 flushed per "
                                        "replay; _no_overlap: the same with programmatic dependent launch off")
     out["decode_step_us_at_M1"] = decode_step(torch, dsnq, inputs, dev, flush, buf, gq, gkv, dec.eps, qo, so, ko)
-    out["gemm_sweep"] = gemm_sweep(torch, dsnq, inputs, dev, flush, hbm_gbs, args)
+    out["gemm_sweep"] = gemm_sweep(torch, dsnq, inputs, dev, flush, hbm_gbs, args, fp8_peak)
+    out["decode_sweep"] = decode_sweep(torch, dsnq, inputs, dev, flush, hbm_gbs)
 
     # -- norm+quant GB/s over M, and the unfused three-kernel sequence at the same M
     sweep = {}
@@ -382,6 +421,31 @@ def side_measurements(torch, dsnq, inputs, dev, flush, hbm_gbs, args):
     return out
 
 
+def decode_sweep(torch, dsnq, inputs, dev, flush, hbm_gbs):
+    """Norm+quant at the decode batch sizes, on strided split views of one
+    [M, 2112] buffer per call, in both scale layouts: us per call in a CUDA
+    graph of 32 calls on 32 distinct cold batches (L2 flushed per replay)."""
+    stream = torch.cuda.current_stream()
+    res = {}
+    for M in (1, 2, 8, 32, 64):
+        dec = inputs.decode_batch(32 * M, seed=1)
+        buf = dec.buf.to(dev)
+        gq, gkv = dec.gamma_q.to(dev), dec.gamma_kv.to(dev)
+        qo = torch.empty(M, KQ, dtype=torch.float8_e4m3fn, device=dev)
+        ko = torch.empty(M, KKV, dtype=torch.bfloat16, device=dev)
+        r = {}
+        for lay in ("row", "col"):
+            so = dsnq.empty_scales(M, KQ // 128, lay, dev)
+            calls = [(lambda i=i: dsnq.fused_dual_rmsnorm_group_quant(
+                buf[i * M:(i + 1) * M, :KQ], buf[i * M:(i + 1) * M, KQ:KQ + KKV], gq, gkv, dec.eps, scale_layout=lay,
+                q_out=qo, q_scale=so, kv_out=ko)) for i in range(32)]
+            r[lay + "_us"] = round(timed_graph_calls(torch, stream, calls, flush), 3)
+        res[str(M)] = r
+    res["note"] = ("us per call: CUDA graph of 32 calls on 32 distinct cold batches of split views (row stride 2112), "
+                   "L2 flushed per replay; row = [M,12] scales, col = [12,M] (transpose_scale)")
+    return res
+
+
 def decode_step(torch, dsnq, inputs, dev, flush, buf, gq, gkv, eps, qo, so, ko):
     """One decode step at M=1 (fused norm+quant, then the dual GEMM on its
     output): a CUDA graph of 8 steps on 8 cold rows, cycling over 4 copies of
@@ -430,7 +494,7 @@ def decode_step(torch, dsnq, inputs, dev, flush, buf, gq, gkv, eps, qo, so, ko):
     return res
 
 
-def gemm_sweep(torch, dsnq, inputs, dev, flush, hbm_gbs, args):
+def gemm_sweep(torch, dsnq, inputs, dev, flush, hbm_gbs, args, fp8_peak):
     """The dual GEMM alone over the decode and full-path batch sizes, with
     pre-quantized activations: us per launch, TFLOP/s and weight-stream GB/s."""
     stream = torch.cuda.current_stream()
@@ -441,7 +505,7 @@ def gemm_sweep(torch, dsnq, inputs, dev, flush, hbm_gbs, args):
     copies = []
     for M in args.gemm_sweep:
         a, sa = inputs.random_codes_and_scales(M, KQ, seed=M)
-        a, sa = a.to(dev), sa.to(dev)
+        a, sa = a.to(dev), sa.to(dev).t().contiguous().t()        # column-major scales, as the path writes them
         oa = torch.empty(M, N_ATTN, dtype=torch.bfloat16, device=dev)
         oi = torch.empty(M, N_IDX, dtype=torch.bfloat16, device=dev)
         us = time_events(torch, stream, lambda: dsnq.block_scaled_fp8_gemm_dual(
@@ -462,8 +526,26 @@ def gemm_sweep(torch, dsnq, inputs, dev, flush, hbm_gbs, args):
             gus = timed_graph_calls(torch, stream, calls, flush, reps=max(args.side_reps, 5))
             res[str(M)].update({"graph_us": round(gus, 3), "graph_gbs": round(byt / (gus * 1e-6) / 1e9, 1),
                                 "graph_frac_hbm": round(byt / (gus * 1e-6) / 1e9 / hbm_gbs, 4)})
-    res["note"] = ("us: one launch timed with CUDA events after an L2 flush (includes launch latency); "
-                   "graph_us: per call in a CUDA graph of 8 back-to-back calls over 4 weight copies (cold in L2)")
+    # Long-context stress: q[32768,1536] with all-zero and single-spike groups,
+    # normalized and quantized by the fused kernel (column-major scales), then
+    # the attention wq_b GEMM (N=24576) on the pair it wrote.
+    if args.long_context:
+        M = 32768
+        lat = inputs.long_context_batch(M, seed=4)
+        q8, s8, _ = dsnq.fused_dual_rmsnorm_group_quant(lat.q.to(dev), lat.kv.to(dev), lat.gamma_q.to(dev),
+                                                        lat.gamma_kv.to(dev), lat.eps, scale_layout="col")
+        oa = torch.empty(M, N_ATTN, dtype=torch.bfloat16, device=dev)
+        us = time_events(torch, stream, lambda: dsnq.block_scaled_fp8_gemm(q8, s8, wa, swa, out=oa), flush,
+                         reps=max(5, args.side_reps // 2))
+        fl = 2.0 * M * N_ATTN * KQ
+        res["32768_long_context_attn"] = {"us": round(us, 3), "tflops": round(fl / (us * 1e-6) / 1e12, 1),
+                                          "frac_fp8": round(fl / (us * 1e-6) / 1e12 / fp8_peak, 4),
+                                          "kernel": "pair_gemm_kernel", "N": N_ATTN}
+        del q8, s8, oa
+    res["note"] = ("column-major activation scales; us: one launch timed with CUDA events after an L2 flush (includes "
+                   "launch latency); graph_us: per call in a CUDA graph of 8 back-to-back calls over 4 weight copies "
+                   "(cold in L2); 32768_long_context_attn: the long-context stress rows quantized by the fused kernel, "
+                   "then the attention wq_b GEMM alone (N=24576)")
     return res
 
 
@@ -565,24 +647,69 @@ def oracle_full_path_sample(rows: int, cols_per_consumer, seed=3, M=8192):
     return time.perf_counter() - t0, flops
 
 
-def blas_threads():
-    try:
-        from threadpoolctl import threadpool_info
-        n = [d.get("num_threads") for d in threadpool_info() if d.get("user_api") == "blas"]
-        if n:
-            return int(max(n))
-    except Exception:
-        pass
-    return len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+def host_cores() -> int:
+    return len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+
+
+_THREAD_ENV = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS",
+               "NUMEXPR_NUM_THREADS")
+
+
+def oracle_child(threads: int, rows: int):
+    """Runs in a child process with a one-thread BLAS pool: the oracle on
+    `rows` rows of the M=8192 full path, spread over `threads` worker threads
+    (numpy releases the GIL in its array operations): the norm+quant by row
+    ranges, the GEMM by 128-row blocks of the weights.  Prints one JSON line."""
+    from concurrent.futures import ThreadPoolExecutor
+    import numpy as np
+    import oracle
+    b, eps, weights = _sample_inputs(rows, None, 3, 8192)
+    t0 = time.perf_counter()
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        parts = list(ex.map(lambda c: oracle.fused_dual_rmsnorm_group_quant(b[0][c], b[1][c], b[2], b[3], eps)[:2],
+                            np.array_split(np.arange(rows), threads)))
+        codes = np.concatenate([p[0] for p in parts])
+        scale = np.concatenate([p[1] for p in parts])
+        flops = 0.0
+        for wc, ws in weights:
+            nb = ws.shape[0]
+            spans = [(int(c[0]), int(c[-1]) + 1) for c in np.array_split(np.arange(nb), min(threads, nb)) if len(c)]
+            outs = list(ex.map(lambda sp: oracle.block_scaled_gemm(codes, scale, wc[sp[0] * 128:sp[1] * 128],
+                                                                   ws[sp[0]:sp[1]]), spans))
+            oracle.output_bf16_bits(np.concatenate(outs, axis=1))
+            flops += 2.0 * rows * wc.shape[0] * KQ
+    secs = time.perf_counter() - t0
+    print(json.dumps({"secs": secs, "flops": flops, "threads": threads}), flush=True)
+
+
+def oracle_timed(threads: int, rows: int):
+    """The oracle timed in a fresh process with `threads` worker threads and a
+    one-thread BLAS pool (a child process, so the pool size is set before
+    numpy loads and nothing is forked from a process that used the GPU)."""
+    env = dict(os.environ)
+    for k in _THREAD_ENV:
+        env[k] = "1"
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-child", str(threads), "--cpu-rows",
+                        str(rows)], capture_output=True, text=True, env=env, cwd=ROOT)
+    if r.returncode != 0:
+        raise RuntimeError(f"oracle child failed: {r.stderr[-2000:]}")
+    return json.loads(r.stdout.strip().splitlines()[-1])
 
 
 def cpu_baseline(rows: int):
-    secs, flops = oracle_full_path_sample(rows, None)
-    return {"value": round(flops / secs / 1e12, 6), "unit": "TFLOP/s", "cores": blas_threads(),
-            "kind": "oracle",
-            "sample": ("all 8192 rows" if rows == 8192 else f"{rows} random rows") + " of the M=8192 full path: "
-                      f"fp64 norm+quant, then the dequantize-"
-                      f"then-fp64 GEMM against all 24576+4096 features ({secs:.1f} s)"}
+    """The fp64 oracle on the host: `rows` random rows of the M=8192 full
+    path (norm+quant, then the GEMM against all 24576+4096 features), once
+    on one thread and once on all the host's cores."""
+    n = host_cores()
+    one = oracle_timed(1, rows)
+    alln = oracle_timed(n, rows)
+    sample = (f"{rows} random rows of the M=8192 full path: fp64 norm+quant, then the dequantize-then-fp64 GEMM "
+              f"against all 24576+4096 features")
+    return {"value": round(alln["flops"] / alln["secs"] / 1e12, 6), "unit": "TFLOP/s", "cores": n, "kind": "oracle",
+            "sample": f"{sample} ({alln['secs']:.1f} s on {n} threads)",
+            "single_thread": {"value": round(one["flops"] / one["secs"] / 1e12, 6), "cores": 1,
+                              "secs": round(one["secs"], 2)}}
 
 
 def run_reference(args, rank, world):
@@ -602,8 +729,8 @@ def run_reference(args, rank, world):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(tot_s / args.steps * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": f"full path M={args.M} (sampled)", "M": args.M},
-        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": blas_threads(),
+        "config": step_config(args.M, world),
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": host_cores(),
                          "kind": "oracle",
                          "sample": f"per step: {rows} random rows x {cols} features of each wq_b, "
                                    f"fp64 norm+quant + dequantize-then-fp64 GEMM"},
@@ -678,12 +805,18 @@ def main():
     ap.add_argument("--nq-sweep", type=int, nargs="*", default=[1024, 8192, 32768])
     ap.add_argument("--side-reps", type=int, default=20)
     ap.add_argument("--gemm-sweep", type=int, nargs="*", default=[1, 8, 64, 128, 1024])
-    ap.add_argument("--cpu-rows", type=int, default=8192)
+    ap.add_argument("--cpu-rows", type=int, default=1024)
+    ap.add_argument("--no-long-context", dest="long_context", action="store_false",
+                    help="skip the M=32768 long-context GEMM of the side measurements")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--kernel-only", choices=["gemm", "norm_quant"], default=None,
                     help="profiling aid: launch one kernel --launches times and exit")
     ap.add_argument("--launches", type=int, default=3)
+    ap.add_argument("--oracle-child", type=int, default=0, help=argparse.SUPPRESS)
     args = ap.parse_args()
+    if args.oracle_child:
+        oracle_child(args.oracle_child, args.cpu_rows)
+        return
     if args.kernel_only:
         run_kernel_only(args)
         return

@@ -61,3 +61,37 @@ def test_peaks_come_from_the_measured_file():
 def test_whole_job_value_counts_every_rank(world):
     # TFLOP/s of all ranks' work over the slowest rank's step time.
     assert bench.whole_job_value(world, 1e12, 2.0) == pytest.approx(world * 1e12 / 2e-3 / 1e12)
+
+
+def test_headline_keeps_the_metric_numbers():
+    """The compact summary printed last on the bench line carries the
+    figures the metric is quoted on."""
+    line = {"roofline": {"achieved": 2000.0, "frac": 0.51}, "roofline_norm_quant": {"frac": 0.4},
+            "norm_quant_us_at_M1": 2.4,
+            "norm_quant_sweep": {"8192": {"fused_graph_frac_hbm": 0.52, "speedup_vs_unfused": 2.5}, "note": "x"},
+            "decode_step_us_at_M1": {"overlap": 13.0},
+            "gemm_sweep": {"1": {"graph_us": 10.8, "graph_frac_hbm": 0.6}, "1024": {"tflops": 1600.0},
+                           "32768_long_context_attn": {"tflops": 2000.0, "frac_fp8": 0.52}},
+            "decode_sweep": {"1": {"row_us": 2.5, "col_us": 2.5}, "note": "x"},
+            "cpu_baseline": {"cores": 16, "value": 0.1, "single_thread": {"value": 0.02}}}
+    h = bench.headline(line)
+    assert h["norm_quant_us_at_M1"] == 2.4
+    assert h["norm_quant_graph_frac_hbm"] == {"8192": 0.52}
+    assert h["gemm_attn_M32768_frac_fp8"] == 0.52 and h["gemm_dual_M8192_frac_fp8"] == 0.51
+    assert h["norm_quant_decode_us"] == {"1": [2.5, 2.5]}
+    assert h["cpu_oracle_tflops"] == {"cores": 16, "all": 0.1, "one_thread": 0.02}
+
+
+def test_both_arms_describe_the_same_workload():
+    assert bench.step_config(8192, 1) == bench.step_config(8192, 1)
+    assert bench.step_config(8192, 1)["M"] == 8192
+
+
+def test_cpu_baseline_times_the_oracle_on_one_and_all_cores():
+    """The oracle runs in child processes (one thread, then all cores) on a
+    small sample here; the line reports both with their core counts."""
+    r = bench.cpu_baseline(8)
+    assert r["kind"] == "oracle" and r["unit"] == "TFLOP/s"
+    assert r["cores"] == bench.host_cores() >= 1
+    assert r["single_thread"]["cores"] == 1
+    assert r["value"] > 0 and r["single_thread"]["value"] > 0
