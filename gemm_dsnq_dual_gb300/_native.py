@@ -11,12 +11,16 @@ import ctypes as C
 import os
 import threading
 
-LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libdsnq.so")
+_PKG = os.path.dirname(os.path.abspath(__file__))
+RELEASE_LIB_PATH = os.path.join(_PKG, "libdsnq.so")
+DEBUG_LIB_PATH = os.path.join(_PKG, "libdsnq_debug.so")      # device index checks (DSNQ_DEBUG)
+# DSNQ_DEBUG=1 in the environment selects the debug build.
+LIB_PATH = DEBUG_LIB_PATH if os.environ.get("DSNQ_DEBUG") == "1" else RELEASE_LIB_PATH
 
 DSNQ_OK = 0
 STATUS_NAMES = {
     0: "DSNQ_OK", 1: "DSNQ_ERR_INVALID_ARG", 2: "DSNQ_ERR_MISALIGNED",
-    3: "DSNQ_ERR_UNSUPPORTED", 4: "DSNQ_ERR_CUDA", 5: "DSNQ_ERR_TIMEOUT",
+    3: "DSNQ_ERR_UNSUPPORTED", 4: "DSNQ_ERR_CUDA", 5: "DSNQ_ERR_TIMEOUT", 6: "DSNQ_ERR_BOUNDS",
 }
 
 i64, i32, u32, u64, f32, vp = C.c_int64, C.c_int32, C.c_uint32, C.c_uint64, C.c_float, C.c_void_p
@@ -59,6 +63,7 @@ SIGNATURES = {
     "dsnq_gemm_plan": (i32, [i64, i64, C.POINTER(C.c_int32), pi64]),
     "dsnq_bf16a_workspace_bytes": (i32, [i64, i64, pi64, pi64]),
     "dsnq_debug_status": (i32, [vp]),
+    "dsnq_debug_build": (i32, []),
     "dsnq_debug_set": (None, [u32, u64]),
     "dsnq_set_launch_overlap": (None, [i32]),
 }
@@ -89,6 +94,14 @@ def lib() -> C.CDLL:
                     fn.argtypes = args
                 _lib = h
     return _lib
+
+
+def use_library(path: str) -> None:
+    """Load `path` (the release or the debug build) for every later call."""
+    global _lib, LIB_PATH
+    with _lock:
+        LIB_PATH = path
+        _lib = None
 
 
 def check(status: int, where: str) -> None:

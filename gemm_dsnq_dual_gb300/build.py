@@ -23,6 +23,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build", platform.machine() or "unknown")
 LIB_NAME = "libdsnq.so"
 LIB_PATH = os.path.join(PKG_DIR, LIB_NAME)
+DEBUG_LIB_PATH = os.path.join(PKG_DIR, "libdsnq_debug.so")   # device index checks (DSNQ_DEBUG)
 
 SOURCES = ["norm_quant.cu", "gemm_fp8.cu", "dsnq_api.cu", "static_scratch.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -54,40 +55,55 @@ def _headers():
     return hs
 
 
-def build(verbose: bool = False, force: bool = False, extra_flags=None) -> str:
-    """Compile and link libdsnq.so; returns its path.  Skips up-to-date work."""
-    os.makedirs(BUILD_DIR, exist_ok=True)
+def _build_one(debug: bool, verbose: bool, force: bool, extra_flags, pool) -> str:
+    variant = "debug" if debug else "release"
+    bdir = os.path.join(BUILD_DIR, variant)
+    os.makedirs(bdir, exist_ok=True)
+    lib_path = DEBUG_LIB_PATH if debug else LIB_PATH
     cc = nvcc()
     headers = _headers()
-    extra = list(extra_flags or [])
+    extra = list(extra_flags or []) + (["-DDSNQ_DEBUG"] if debug else [])
 
     def compile_one(src: str) -> str:
         s = os.path.join(CSRC, src)
-        o = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))
+        o = os.path.join(bdir, src.replace(".cu", ".o"))
         if force or not _newer(o, [s, *headers, __file__]):
             cmd = [cc, *ARCH, *FLAGS, *extra, "-c", s, "-o", o]
             if verbose:
                 print(" ".join(cmd), flush=True)
             r = subprocess.run(cmd, capture_output=True, text=True)
             if r.returncode != 0:
-                raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")
+                raise RuntimeError(f"nvcc failed on {src} ({variant}):\n{r.stdout}\n{r.stderr}")
             if verbose and r.stderr:
                 print(r.stderr, file=sys.stderr)
         return o
 
-    with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        objs = list(ex.map(compile_one, SOURCES))
-    stamp = os.path.join(BUILD_DIR, "libdsnq.stamp")   # which objects the library was linked from
-    if force or not _newer(LIB_PATH, objs) or not os.path.exists(stamp) or \
-            open(stamp).read() != LIB_PATH + "\n" + platform.machine():
-        cmd = [cc, *ARCH, "-shared", "-o", LIB_PATH + ".tmp", *objs, "-lcudart"]
+    objs = list(pool.map(compile_one, SOURCES))
+    stamp = os.path.join(bdir, "libdsnq.stamp")   # which objects the library was linked from
+    if force or not _newer(lib_path, objs) or not os.path.exists(stamp) or \
+            open(stamp).read() != lib_path + "\n" + platform.machine():
+        cmd = [cc, *ARCH, "-shared", "-o", lib_path + ".tmp", *objs, "-lcudart"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-        os.replace(LIB_PATH + ".tmp", LIB_PATH)
+        os.replace(lib_path + ".tmp", lib_path)
         with open(stamp, "w") as f:
-            f.write(LIB_PATH + "\n" + platform.machine())
-    return LIB_PATH
+            f.write(lib_path + "\n" + platform.machine())
+    return lib_path
+
+
+def build(verbose: bool = False, force: bool = False, extra_flags=None, debug: bool = True) -> str:
+    """Compile and link libdsnq.so (and, with debug=True, libdsnq_debug.so:
+    the same sources with the device index checks of DSNQ_DEBUG); returns the
+    release library's path.  Skips up-to-date work."""
+    # Two builders, each compiling its sources on a shared pool of nvcc jobs
+    # (the builders only wait; the compiles run on the other pool).
+    with ThreadPoolExecutor(max_workers=2 * len(SOURCES)) as cc_pool, ThreadPoolExecutor(max_workers=2) as libs:
+        jobs = [libs.submit(_build_one, False, verbose, force, extra_flags, cc_pool)]
+        if debug:
+            jobs.append(libs.submit(_build_one, True, verbose, force, extra_flags, cc_pool))
+        paths = [j.result() for j in jobs]
+    return paths[0]
 
 
 if __name__ == "__main__":

@@ -15,6 +15,7 @@ extern "C" const char* dsnq_status_string(dsnq_status status) {
         case DSNQ_ERR_UNSUPPORTED: return "DSNQ_ERR_UNSUPPORTED";
         case DSNQ_ERR_CUDA: return "DSNQ_ERR_CUDA";
         case DSNQ_ERR_TIMEOUT: return "DSNQ_ERR_TIMEOUT";
+        case DSNQ_ERR_BOUNDS: return "DSNQ_ERR_BOUNDS";
     }
     return "DSNQ_ERR_UNKNOWN";
 }
@@ -23,9 +24,26 @@ extern "C" int32_t dsnq_version(void) { return 100; }  // 0.1.0
 
 namespace {
 std::atomic<int> g_launch_overlap{1};
+std::atomic<uint32_t> g_inject{0};
+std::atomic<uint64_t> g_timeout_ns{0};
 }
 
 bool dsnq::launch_overlap_enabled() { return g_launch_overlap.load(std::memory_order_relaxed) != 0; }
+uint32_t dsnq::debug_inject_flags() { return g_inject.load(std::memory_order_relaxed); }
+uint64_t dsnq::debug_wait_timeout_ns() { return g_timeout_ns.load(std::memory_order_relaxed); }
+
+extern "C" void dsnq_debug_set(uint32_t inject_flags, uint64_t wait_timeout_ns) {
+    g_inject.store(inject_flags);
+    g_timeout_ns.store(wait_timeout_ns);
+}
+
+extern "C" int32_t dsnq_debug_build(void) {
+#ifdef DSNQ_DEBUG
+    return 1;
+#else
+    return 0;
+#endif
+}
 
 extern "C" void dsnq_set_launch_overlap(int32_t enable) {
     g_launch_overlap.store(enable ? 1 : 0, std::memory_order_relaxed);

@@ -9,6 +9,21 @@
 
 namespace dsnq {
 
+// Bits of the device status words read by dsnq_debug_status.
+constexpr uint32_t kStatusTimeout = 1u;   // a bounded wait gave up
+constexpr uint32_t kStatusBounds = 2u;    // a debug-build index check failed
+
+// Test-hook flags (dsnq_debug_set).
+constexpr uint32_t kInjectSkipLoad = 1u;          // the GEMM producer skips its first load
+constexpr uint32_t kInjectBoundsSelfTest = 2u;    // debug build: one deliberate failed index check
+
+// Test hooks and the wait bound, set by dsnq_debug_set (dsnq_api.cu).
+uint32_t debug_inject_flags();
+uint64_t debug_wait_timeout_ns();
+
+// The status word of the norm+quant unit, read and cleared (norm_quant.cu).
+bool take_norm_quant_debug_word(cudaStream_t s, unsigned int* v);
+
 inline bool aligned(const void* p, uintptr_t a) {
     return (reinterpret_cast<uintptr_t>(p) % a) == 0;
 }

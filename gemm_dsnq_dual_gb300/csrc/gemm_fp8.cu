@@ -54,6 +54,7 @@
 #include <tuple>
 #include <vector>
 
+#include "debug_check.cuh"
 #include "dsnq_internal.h"
 #include "group_quant.cuh"
 
@@ -63,9 +64,7 @@ namespace gemm {
 constexpr int kBK = 128;            // K bytes per stage = one scale block
 constexpr int kUmmaK = 32;          // K per tcgen05.mma kind::f8f6f4
 constexpr int kPRows = 128;         // MMA M
-constexpr uint32_t kStatusTimeout = 1u;
-
-__device__ unsigned int g_status;   // device status word (bit 0: a wait timed out)
+__device__ unsigned int g_status;   // device status word (kStatusTimeout: a wait timed out)
 
 struct Problem {
     int N;
@@ -492,10 +491,12 @@ __device__ __forceinline__ void zero_rows(int KB, int live, uint8_t* a_res, floa
     const int zero_vec = (BN - live) * (kBK / 16);          // uint4 per K block
     for (int e = qw * 32 + lane; e < KB * zero_vec; e += nw * 32) {
         const int kb = e / zero_vec, v = e % zero_vec;
-        reinterpret_cast<uint4*>(a_res + kb * (BN * kBK) + live * kBK)[v] = make_uint4(0, 0, 0, 0);
+        if (bounds_ok(kb < KB && live * kBK + 16 * (v + 1) <= BN * kBK))
+            reinterpret_cast<uint4*>(a_res + kb * (BN * kBK) + live * kBK)[v] = make_uint4(0, 0, 0, 0);
     }
     for (int e = qw * 32 + lane; e < KB * (BN - live); e += nw * 32) {
         const int kb = e / (BN - live), r = live + e % (BN - live);
+        if (!bounds_ok(kb < KB && r < BN && kb * BN + r < slot_stride)) continue;
         sa_slots[kb * BN + r] = 0.f;
         sa_slots[slot_stride + kb * BN + r] = 0.f;
     }
@@ -524,7 +525,7 @@ __device__ __forceinline__ void quantize_activations(const Params& p, uint8_t* a
             kb[j] = 2 * slot + h;
             on[j] = u < units && kb[j] < KB;    // odd KB: the last slot's second half is past the row
             raw[j] = make_uint4(0, 0, 0, 0);
-            if (on[j])
+            if (on[j] && bounds_ok(row[j] < p.M && (slot * 32 + lane) * 8 + 8 <= p.K))
                 raw[j] = __ldg(reinterpret_cast<const uint4*>(p.a_bf16 + static_cast<int64_t>(row[j]) * p.lda_bf16 +
                                                                (slot * 32 + lane) * 8));
         }
@@ -549,6 +550,7 @@ __device__ __forceinline__ void quantize_activations(const Params& p, uint8_t* a
             uint2 codes = quant8_bracket(x[j], gq, ok);
             if (!ok) codes = quant8_divide(x[j], gq.scale);
             const int r = row[j];
+            if (!bounds_ok(r < BN && kb[j] < KB && kb[j] * BN + r < slot_stride)) continue;
             *reinterpret_cast<uint2*>(a_res + kb[j] * (BN * kBK) + r * kBK + ((c16 ^ (r & 7)) << 4) + (lane & 1) * 8) =
                 codes;
             if ((lane & 15) == 0) {
@@ -589,7 +591,7 @@ __device__ __forceinline__ void norm_quantize_activations(const Params& p, uint8
 #pragma unroll
         for (int i = 0; i < kMaxSlots; ++i) {
             raw[i] = graw[i] = make_uint4(0, 0, 0, 0);
-            if (i < slots && 2 * i + h < KB) {
+            if (i < slots && 2 * i + h < KB && bounds_ok(m < p.M && (i * 32 + lane) * 8 + 8 <= K)) {
                 raw[i] = __ldg(reinterpret_cast<const uint4*>(row + (i * 32 + lane) * 8));
                 graw[i] = __ldg(reinterpret_cast<const uint4*>(p.gamma_q + (i * 32 + lane) * 8));
             }
@@ -630,6 +632,7 @@ __device__ __forceinline__ void norm_quantize_activations(const Params& p, uint8
             for (int j = 0; j < kU; ++j) {
                 const int i = i0 + j, kb = 2 * i + h;
                 if (i >= slots || kb >= KB) continue;
+                if (!bounds_ok(m < BN && m < p.M && kb * BN + m < slot_stride)) continue;
                 const GroupQuant gq = make_group_quant(amax[j]);
                 bool ok;
                 uint2 codes = quant8_bracket(x[j], gq, ok);
@@ -640,7 +643,7 @@ __device__ __forceinline__ void norm_quantize_activations(const Params& p, uint8
                     sa_slots[kb * BN + m] = gq.scale;
                     sa_slots[slot_stride + kb * BN + m] = gq.scale;
                 }
-                if (side && p.q_out)
+                if (side && p.q_out && bounds_ok((i * 32 + lane) * 8 + 8 <= K))
                     *reinterpret_cast<uint2*>(p.q_out + static_cast<int64_t>(m) * K + (i * 32 + lane) * 8) = codes;
                 if (side && p.qs_out && (lane & 15) == 0) p.qs_out[static_cast<int64_t>(kb) * p.M + m] = gq.scale;
             }
@@ -659,7 +662,7 @@ __device__ __forceinline__ void norm_kv_rows(const Params& p, int qw, int nw, in
 #pragma unroll
         for (int i = 0; i < kMaxSlots; ++i) {
             raw[i] = graw[i] = make_uint4(0, 0, 0, 0);
-            if (i * 32 + lane < kchunks) {
+            if (i * 32 + lane < kchunks && bounds_ok(m < p.M)) {
                 raw[i] = __ldg(reinterpret_cast<const uint4*>(krow + (i * 32 + lane) * 8));
                 graw[i] = __ldg(reinterpret_cast<const uint4*>(p.gamma_kv + (i * 32 + lane) * 8));
             }
@@ -689,7 +692,8 @@ __device__ __forceinline__ void norm_kv_rows(const Params& p, int qw, int nw, in
                 const float2 y = mul2(mul2(x[t], rk2), g[t]);
                 hv[t] = __floats2bfloat162_rn(y.x, y.y);
             }
-            *reinterpret_cast<uint4*>(p.kv_out + static_cast<int64_t>(m) * p.ldkv_out + (i * 32 + lane) * 8) = v;
+            if (bounds_ok(m < p.M && (i * 32 + lane) * 8 + 8 <= p.kkv))
+                *reinterpret_cast<uint4*>(p.kv_out + static_cast<int64_t>(m) * p.ldkv_out + (i * 32 + lane) * 8) = v;
         }
     }
 }
@@ -800,6 +804,7 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
     // reads inputs (or writes outputs that an earlier kernel may still read).
     grid_dependency_wait();
     allow_dependent_launch();
+    bounds_self_test(p.inject);
 
     if (AQ && warp >= 2) {
         // Quantize the activations once for all of this CTA's tiles, while the
@@ -935,6 +940,7 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                 constexpr int kVec = C::kScaleCols / 4;
                 for (int e = lane; e < KB * kVec; e += 32) {
                     const int kb = e / kVec, v = e % kVec;
+                    if (!bounds_ok(m0 + 4 * v + 4 <= p.M && kb * C::kScaleCols + 4 * v + 4 <= KBP * C::kScaleCols)) continue;
                     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(sa_dst + kb * C::kScaleCols + 4 * v)),
                                  "l"(p.a_scale + static_cast<int64_t>(kb) * p.as_gs + m0 + 4 * v)
                                  : "memory");
@@ -945,11 +951,13 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                     const int m = m0 + j;
                     const bool live = m < p.M;                 // zero fill past the last row
                     const float* src = live ? p.a_scale + static_cast<int64_t>(m) * p.as_rs + kb * p.as_gs : p.a_scale;
+                    if (!bounds_ok(e < KBP * C::kScaleCols)) continue;
                     asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(sa_dst + e)), "l"(src),
                                  "r"(live ? 4 : 0)
                                  : "memory");
                 }
             }
+            if (!bounds_ok(n0 / kPRows < (pr.N + kPRows - 1) / kPRows)) break;
             for (int kb = lane; kb < KB; kb += 32)
                 asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(sw_slots + slot * KBP + kb)),
                              "l"(sw + kb)
@@ -992,6 +1000,7 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
             // loads are slow while the tensor core streams its operands.
             auto promote = [&](const float2* sc, bool uniform) -> bool {
                 const int b = g % NBUF;
+                if (!bounds_ok(b * BN + col0 + C::kCols <= C::kTmemCols)) return false;
                 // Every lane polls (each acquires the phase); the outcome is made
                 // warp-uniform before the warp-collective TMEM load.
                 const bool got = wait_bounded<true>(smem_u32(&tfull[b]), (g / NBUF) & 1, abort_flag, tmo);
@@ -1102,7 +1111,8 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                     for (int j = 0; j < C::kCols; ++j) {
                         const int m = m0 + col0 + j;
                         const float v = (j & 1) ? acc[j / 2].y : acc[j / 2].x;
-                        if (m < p.M) pr.out[static_cast<int64_t>(m) * pr.ldo + n] = __float2bfloat16_rn(v);
+                        if (m < p.M && bounds_ok(m >= 0 && n >= 0 && n < pr.N))
+                            pr.out[static_cast<int64_t>(m) * pr.ldo + n] = __float2bfloat16_rn(v);
                     }
                 }
             }
@@ -1331,6 +1341,7 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
     const uint64_t tmo = p.timeout_ns;
     grid_dependency_wait();      // as in block_scaled_gemm_kernel
     allow_dependent_launch();
+    bounds_self_test(p.inject);
 
     // Warp-group 0 (the role warps) hands registers to the promotion warps.
     if (warp < 4) {
@@ -1449,6 +1460,7 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
             if (p.vec_scales && rows >= kPRows) {
                 for (int e = lane; e < KB * (kPRows / 4); e += 32) {
                     const int kb = e / (kPRows / 4), v = e % (kPRows / 4);
+                    if (!bounds_ok(m0 + 4 * v + 4 <= p.M && kb < KBP)) continue;
                     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(sa_dst + kb * kPRows + 4 * v)),
                                  "l"(p.a_scale + static_cast<int64_t>(kb) * p.as_gs + m0 + 4 * v)
                                  : "memory");
@@ -1459,6 +1471,7 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
                     const int m = m0 + j;
                     const bool live = m < p.M;
                     const float* src = live ? p.a_scale + static_cast<int64_t>(m) * p.as_rs + kb * p.as_gs : p.a_scale;
+                    if (!bounds_ok(e < KBP * kPRows)) continue;
                     asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(sa_dst + e)), "l"(src),
                                  "r"(live ? 4 : 0)
                                  : "memory");
@@ -1525,6 +1538,10 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
                 }
                 tc_fence_after();
                 const float2 s2 = make_float2(sk, sk);
+                if (!bounds_ok((2 * half + b) * kHalfN + hcol + kCols <= kTmemCols)) {
+                    ok = false;
+                    break;
+                }
                 const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                        static_cast<uint32_t>((2 * half + b) * kHalfN + hcol);
                 // Four 16-column loads, each issued while the previous chunk is
@@ -1738,8 +1755,6 @@ bool set_smem_attr(const void* kern, size_t smem) {
     return true;
 }
 
-std::atomic<uint32_t> g_inject{0};
-std::atomic<uint64_t> g_timeout_ns{0};
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
 
 struct Consumer {
@@ -2014,9 +2029,9 @@ dsnq_status run_gemm(int64_t M, int64_t K, const void* a, int64_t lda, const flo
     if (total > 0x7fffffffLL) return DSNQ_ERR_UNSUPPORTED;
     prm.total_tiles = static_cast<int>(total);
     prm.total_super = static_cast<int>(total_super);
-    const uint64_t tmo = g_timeout_ns.load();
+    const uint64_t tmo = debug_wait_timeout_ns();
     prm.timeout_ns = tmo ? tmo : kDefaultTimeoutNs;
-    prm.inject = g_inject.load();
+    prm.inject = debug_inject_flags();
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     switch (variant) {
@@ -2159,7 +2174,7 @@ extern "C" dsnq_status dsnq_fused_norm_quant_gemm_dual(
 
 extern "C" dsnq_status dsnq_debug_status(void* stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    unsigned int v = 0;
+    unsigned int v = 0, w = 0, n = 0;
     if (cudaMemcpyFromSymbolAsync(&v, gemm::g_status, sizeof(v), 0, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
         cudaStreamSynchronize(s) != cudaSuccess) {
         cudaGetLastError();
@@ -2171,10 +2186,9 @@ extern "C" dsnq_status dsnq_debug_status(void* stream) {
         cudaGetLastError();
         return DSNQ_ERR_CUDA;
     }
-    return (v & gemm::kStatusTimeout) ? DSNQ_ERR_TIMEOUT : DSNQ_OK;
-}
-
-extern "C" void dsnq_debug_set(uint32_t inject_flags, uint64_t wait_timeout_ns) {
-    g_inject.store(inject_flags);
-    g_timeout_ns.store(wait_timeout_ns);
+    // The index-check words of this unit and of the norm+quant unit.
+    if (!take_debug_word(s, &w) || !take_norm_quant_debug_word(s, &n)) return DSNQ_ERR_CUDA;
+    v |= w | n;
+    if (v & kStatusTimeout) return DSNQ_ERR_TIMEOUT;
+    return (v & kStatusBounds) ? DSNQ_ERR_BOUNDS : DSNQ_OK;
 }

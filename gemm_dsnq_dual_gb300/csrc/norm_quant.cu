@@ -29,6 +29,7 @@
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
+#include "debug_check.cuh"
 #include "dsnq_internal.h"
 #include "group_quant.cuh"
 
@@ -63,6 +64,7 @@ struct RowArgs {
     int64_t scale_row_stride, scale_group_stride;  // (m, g) at m*rs + g*gs
     __nv_bfloat16* kv_out;
     int64_t ldkv_out;
+    uint32_t inject;       // test hooks (dsnq_debug_set)
 };
 
 __device__ __forceinline__ uint4 pack8_bf16(const float2 (&f)[4]) {
@@ -136,6 +138,7 @@ __global__ void __launch_bounds__(kThreads, min_blocks_per_sm(PASSES))
 row_norm_quant_kernel(const RowArgs a) {
     grid_dependency_wait();      // inputs are read only once the previous kernel's writes are visible
     allow_dependent_launch();
+    bounds_self_test(a.inject);
     const int t = threadIdx.x;
     const int lane = t & 31, warp = t >> 5;
 
@@ -164,7 +167,7 @@ row_norm_quant_kernel(const RowArgs a) {
 #pragma unroll
         for (int p = 0; p < PASSES; ++p) {
             raw[p] = make_uint4(0, 0, 0, 0);
-            if (live[p]) {
+            if (live[p] && bounds_ok(m < a.M && col[p] + kChunk <= (is_q[p] ? a.cq : a.ckv) * kChunk)) {
                 const __nv_bfloat16* src = is_q[p] ? a.q + m * a.ldq + col[p] : a.kv + m * a.ldkv + col[p];
                 raw[p] = __ldg(reinterpret_cast<const uint4*>(src));
             }
@@ -216,8 +219,11 @@ row_norm_quant_kernel(const RowArgs a) {
 
 #pragma unroll
         for (int p = 0; p < PASSES; ++p) {
+            // Debug build: a chunk whose indices fail the check stores nothing
+            // (it still takes part in the warp's shuffles).
+            const bool in = bounds_ok(m < a.M && (!live[p] || col[p] + kChunk <= (is_q[p] ? a.cq : a.ckv) * kChunk));
             if (MODE == kNormOnly) {
-                if (!live[p]) continue;
+                if (!live[p] || !in) continue;
                 if (is_q[p])
                     *reinterpret_cast<uint4*>(a.q_bf16 + m * a.ldq_out + col[p]) = pack8_bf16(x[p]);
                 else
@@ -230,7 +236,7 @@ row_norm_quant_kernel(const RowArgs a) {
 #pragma unroll
             for (int i = 0; i < 4; ++i) amax = fmaxf(amax, fmaxf(fabsf(x[p][i].x), fabsf(x[p][i].y)));
             amax = half_warp_max(amax);
-            if (!live[p]) continue;
+            if (!live[p] || !in) continue;
             if (is_q[p]) {
                 const QuantScale qs = make_quant_scale(amax);
                 *reinterpret_cast<uint2*>(a.q_fp8 + m * a.ldq_out + col[p]) = pack8_e4m3(x[p], qs);
@@ -260,6 +266,7 @@ __global__ void __launch_bounds__(kRowWarps * 32, kRowCtasPerSM)
 warp_row_kernel(const RowArgs a) {
     grid_dependency_wait();      // inputs are read only once the previous kernel's writes are visible
     allow_dependent_launch();
+    bounds_self_test(a.inject);
     extern __shared__ float gamma_s[];          // [Kq + Kkv] fp32
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -279,7 +286,7 @@ warp_row_kernel(const RowArgs a) {
 #pragma unroll
         for (int j = 0; j < CPT; ++j) {
             raw[j] = make_uint4(0, 0, 0, 0);
-            if (live[j]) {
+            if (live[j] && bounds_ok(m < a.M && col[j] + kChunk <= (is_q[j] ? a.cq : a.ckv) * kChunk)) {
                 const __nv_bfloat16* src = is_q[j] ? a.q + m * a.ldq + col[j] : a.kv + m * a.ldkv + col[j];
                 raw[j] = __ldg(reinterpret_cast<const uint4*>(src));
             }
@@ -331,6 +338,9 @@ warp_row_kernel(const RowArgs a) {
 
 #pragma unroll
         for (int j = 0; j < CPT; ++j) {
+            // Debug build: a chunk whose indices fail the check stores nothing
+            // (it still takes part in the warp's votes and shuffles).
+            const bool in = bounds_ok(m < a.M && (!live[j] || col[j] + kChunk <= (is_q[j] ? a.cq : a.ckv) * kChunk));
             float2 x[4];
             unpack8(cur[j], x);
             if (MODE != kQuantOnly) {
@@ -345,7 +355,7 @@ warp_row_kernel(const RowArgs a) {
                 x[3] = mul2(mul2(x[3], r2), make_float2(g1.z, g1.w));
             }
             if (MODE == kNormOnly) {
-                if (!live[j]) continue;
+                if (!live[j] || !in) continue;
                 if (is_q[j])
                     *reinterpret_cast<uint4*>(a.q_bf16 + m * a.ldq_out + col[j]) = pack8_bf16(x);
                 else
@@ -359,6 +369,7 @@ warp_row_kernel(const RowArgs a) {
                 for (int i = 0; i < 4; ++i) amax = fmaxf(amax, fmaxf(fabsf(x[i].x), fabsf(x[i].y)));
                 amax = half_warp_max(amax);
                 if (is_q[j]) {
+                    if (!in) continue;
                     const QuantScale qs = make_quant_scale(amax);
                     *reinterpret_cast<uint2*>(a.q_fp8 + m * a.ldq_out + col[j]) = pack8_e4m3(x, qs);
                     if ((lane & 15) == 0)
@@ -366,7 +377,7 @@ warp_row_kernel(const RowArgs a) {
                     continue;
                 }
             }
-            if (MODE == kFused && live[j])
+            if (MODE == kFused && live[j] && in)
                 *reinterpret_cast<uint4*>(a.kv_out + m * a.ldkv_out + col[j]) = pack8_bf16(x);
         }
 #pragma unroll
@@ -402,6 +413,7 @@ warp_row_fused_kernel(const RowArgs a) {
     static_assert(QS == 6 && KS == 2, "the lane roles below are laid out for the DSv4 row");
     grid_dependency_wait();      // inputs are read only once the previous kernel's writes are visible
     allow_dependent_launch();
+    bounds_self_test(a.inject);
     constexpr int CPT = QS + KS;
     constexpr unsigned kAll = 0xffffffffu;
     extern __shared__ float gamma_s[];          // [(QS + KS) * 256] fp32: gamma_q then gamma_kv
@@ -416,9 +428,11 @@ warp_row_fused_kernel(const RowArgs a) {
     auto load_row = [&](int64_t m, uint4 (&raw)[CPT]) {
         const __nv_bfloat16* qrow = a.q + m * a.ldq + lane * kChunk;
         const __nv_bfloat16* kvrow = a.kv + m * a.ldkv + lane * kChunk;
+        const bool in = bounds_ok(m < a.M && a.cq == QS * 32 && a.ckv == KS * 32);
 #pragma unroll
         for (int j = 0; j < CPT; ++j)
-            raw[j] = __ldg(reinterpret_cast<const uint4*>(j < QS ? qrow + j * 256 : kvrow + (j - QS) * 256));
+            raw[j] = in ? __ldg(reinterpret_cast<const uint4*>(j < QS ? qrow + j * 256 : kvrow + (j - QS) * 256))
+                        : make_uint4(0, 0, 0, 0);
     };
 
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kRowWarps;
@@ -482,7 +496,8 @@ warp_row_fused_kernel(const RowArgs a) {
             x[j][1] = mul2(mul2(x[j][1], r2), make_float2(g0.z, g0.w));
             x[j][2] = mul2(mul2(x[j][2], r2), make_float2(g1.x, g1.y));
             x[j][3] = mul2(mul2(x[j][3], r2), make_float2(g1.z, g1.w));
-            if (j >= QS) *reinterpret_cast<uint4*>(a.kv_out + m * a.ldkv_out + col) = pack8_bf16(x[j]);
+            if (j >= QS && bounds_ok(m < a.M && col + kChunk <= a.ckv * kChunk))
+                *reinterpret_cast<uint4*>(a.kv_out + m * a.ldkv_out + col) = pack8_bf16(x[j]);
         }
 
         // Group maxima: this lane's eight values per q slot, then the
@@ -508,7 +523,8 @@ warp_row_fused_kernel(const RowArgs a) {
         const float own_y = group_recip(own_scale);
         if (gi < 3) {
             const int g = 2 * (3 * (hi8 ? 1 : 0) + gi) + h;
-            a.scale[m * a.scale_row_stride + g * a.scale_group_stride] = own_scale;
+            if (bounds_ok(g < a.cq / 16 && m < a.M))
+                a.scale[m * a.scale_row_stride + g * a.scale_group_stride] = own_scale;
         }
 
         // Codes, three q slots at a time (fewer live registers).
@@ -539,13 +555,16 @@ warp_row_fused_kernel(const RowArgs a) {
             }
             uint8_t* crow = a.q_fp8 + m * a.ldq_out + lane * kChunk;
 #pragma unroll
-            for (int u = 0; u < kGrp; ++u) *reinterpret_cast<uint2*>(crow + (j0 + u) * 256) = codes[u];
+            for (int u = 0; u < kGrp; ++u)
+                if (bounds_ok(m < a.M && (j0 + u) * 256 + lane * kChunk + kChunk <= a.cq * kChunk))
+                    *reinterpret_cast<uint2*>(crow + (j0 + u) * 256) = codes[u];
         }
     }
 }
 
 template <int MODE>
 static dsnq_status launch_rows(RowArgs a, int64_t M, cudaStream_t s) {
+    a.inject = debug_inject_flags();
     const int chunks = a.cq + a.ckv;
     const int passes = (chunks + kThreads - 1) / kThreads;
     a.M = M;
@@ -603,14 +622,15 @@ static dsnq_status launch_rows(RowArgs a, int64_t M, cudaStream_t s) {
 __global__ void __launch_bounds__(256)
 weight_block_quant_kernel(int64_t N, int64_t K, const float* __restrict__ w, int64_t ldw,
                           uint8_t* __restrict__ out, int64_t ldo,
-                          float* __restrict__ sw, int64_t ldsw) {
+                          float* __restrict__ sw, int64_t ldsw, uint32_t debug_inject) {
     grid_dependency_wait();      // inputs are read only once the previous kernel's writes are visible
     allow_dependent_launch();
+    bounds_self_test(debug_inject);
     const int64_t nb = blockIdx.y, kb = blockIdx.x;
     const int t = threadIdx.x;
     const int64_t row = nb * 128 + t / 2;
     const int64_t c0 = kb * 128 + (t & 1) * 64;
-    const bool live = row < N;
+    const bool live = row < N && bounds_ok(c0 + 64 <= K);
     float v[64];
     float amax = 0.f;
 #pragma unroll
@@ -629,7 +649,7 @@ weight_block_quant_kernel(int64_t N, int64_t K, const float* __restrict__ w, int
 #pragma unroll
     for (int i = 1; i < 8; ++i) amax = fmaxf(amax, red[i]);
     const QuantScale qs = make_quant_scale(amax);
-    if (t == 0) sw[nb * ldsw + kb] = qs.scale;
+    if (t == 0 && bounds_ok(nb * 128 < N && (kb + 1) * 128 <= K)) sw[nb * ldsw + kb] = qs.scale;
     if (!live) return;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {  // 16 codes per 16-byte store
@@ -643,6 +663,8 @@ weight_block_quant_kernel(int64_t N, int64_t K, const float* __restrict__ w, int
         *reinterpret_cast<uint4*>(out + row * ldo + c0 + 16 * j) = make_uint4(lo.x, lo.y, hi.x, hi.y);
     }
 }
+
+bool take_norm_quant_debug_word(cudaStream_t s, unsigned int* v) { return take_debug_word(s, v); }
 
 }  // namespace dsnq
 
@@ -816,5 +838,6 @@ extern "C" dsnq_status dsnq_quantize_weight_block128(
     dim3 grid(static_cast<unsigned>(K / 128), static_cast<unsigned>(nb));
     return launch_result(launch_kernel(weight_block_quant_kernel, grid, dim3(256), 0,
                                        static_cast<cudaStream_t>(stream), N, K, w, ldw,
-                                       static_cast<uint8_t*>(w_fp8), ldw_out, w_scale, ld_wscale));
+                                       static_cast<uint8_t*>(w_fp8), ldw_out, w_scale, ld_wscale,
+                                       debug_inject_flags()));
 }

@@ -53,7 +53,8 @@ typedef enum {
     DSNQ_ERR_MISALIGNED = 2,    /* base or stride not aligned as the call requires */
     DSNQ_ERR_UNSUPPORTED = 3,   /* a valid request outside the shapes implemented */
     DSNQ_ERR_CUDA = 4,          /* the CUDA runtime reported an error */
-    DSNQ_ERR_TIMEOUT = 5        /* a bounded device wait gave up (see dsnq_debug_status) */
+    DSNQ_ERR_TIMEOUT = 5,       /* a bounded device wait gave up (see dsnq_debug_status) */
+    DSNQ_ERR_BOUNDS = 6         /* debug build: a device index check failed (see dsnq_debug_status) */
 } dsnq_status;
 
 /* Scale layout of the per-1x128 activation scales, logical shape [M, G]
@@ -376,12 +377,20 @@ DSNQ_API dsnq_status dsnq_fused_norm_quant_gemm_dual(
     void* stream);
 
 /*
- * Device status word.  Kernels with bounded waits (the GEMM's mbarrier
- * waits) record a timeout there instead of hanging.  This call synchronizes
- * `stream`, reads the word of the current device, clears it and returns
- * DSNQ_OK, DSNQ_ERR_TIMEOUT, or DSNQ_ERR_CUDA if the synchronize failed.
+ * Device status words.  Kernels with bounded waits (the GEMM's mbarrier
+ * waits) record a timeout there instead of hanging.  In the debug build
+ * (libdsnq_debug.so, compiled with DSNQ_DEBUG) every kernel also checks the
+ * indices of its memory accesses against the buffer extents its arguments
+ * describe; a failed check skips the access and records a bounds error.
+ * This call synchronizes `stream`, reads the words of the current device,
+ * clears them and returns DSNQ_OK, DSNQ_ERR_TIMEOUT, DSNQ_ERR_BOUNDS (a
+ * timeout takes precedence when both are recorded), or DSNQ_ERR_CUDA if the
+ * synchronize failed.  No counterpart in the published method.
  */
 DSNQ_API dsnq_status dsnq_debug_status(void* stream);
+
+/* 1 when this library is the debug build (device index checks), else 0. */
+DSNQ_API int32_t dsnq_debug_build(void);
 
 /*
  * Launch overlap (programmatic dependent launch), on by default; affects
@@ -398,11 +407,13 @@ DSNQ_API dsnq_status dsnq_debug_status(void* stream);
 DSNQ_API void dsnq_set_launch_overlap(int32_t enable);
 
 /*
- * Test hooks for the bounded waits (affect later launches on all devices of
- * this process).  wait_timeout_ns bounds every device wait (0 restores the
- * default of 2 s).  inject_flags bit 0 makes the GEMM's producer skip the
- * first stage's load, so the consumer's wait on it must run out: the kernel
- * then records DSNQ_ERR_TIMEOUT, releases its tensor memory and returns.
+ * Test hooks (affect later launches on all devices of this process).
+ * wait_timeout_ns bounds every device wait (0 restores the default of 2 s).
+ * inject_flags bit 0 makes the GEMM's producer skip the first stage's load,
+ * so the consumer's wait on it must run out: the kernel then records
+ * DSNQ_ERR_TIMEOUT, releases its tensor memory and returns.  Bit 1 (debug
+ * build only; ignored otherwise) makes every launch record one failed index
+ * check that guards no access, to test the reporting path.
  */
 DSNQ_API void dsnq_debug_set(uint32_t inject_flags, uint64_t wait_timeout_ns);
 

@@ -38,11 +38,24 @@ def test_every_declared_symbol_is_exported(lib):
         assert hasattr(lib, name), name
 
 
+def test_debug_build_exports_the_same_symbols():
+    """The debug build (device index checks) has the same C ABI."""
+    import ctypes
+    if not os.path.exists(_native.DEBUG_LIB_PATH):
+        build.build()
+    h = ctypes.CDLL(_native.DEBUG_LIB_PATH)
+    for name in declared_functions():
+        assert hasattr(h, name), name
+    h.dsnq_debug_build.restype = ctypes.c_int32
+    assert h.dsnq_debug_build() == 1
+
+
 def test_status_strings_and_version(lib):
     for s, name in _native.STATUS_NAMES.items():
         assert lib.dsnq_status_string(s).decode() == name
     assert lib.dsnq_status_string(99).decode() == "DSNQ_ERR_UNKNOWN"
     assert lib.dsnq_version() >= 100
+    assert lib.dsnq_debug_build() == 0          # the release build
 
 
 def test_quant_output_sizes(lib):

@@ -32,9 +32,16 @@ def test_static_scratch_equals_workspace(M, K):
     o2 = torch.empty(M, 256, dtype=torch.bfloat16, device="cuda")
     torch.cuda.synchronize()
     before = torch.cuda.memory_allocated()
-    dsnq.block_scaled_fp8_gemm_dual_bf16a_static(a, *W, out1=o1, out2=o2)
+    dsnq.block_scaled_fp8_gemm_dual_bf16a_static(a, *W, out1=o1, out2=o2)   # may load the device code
     torch.cuda.synchronize()
     assert torch.cuda.memory_allocated() == before       # no tensor allocated for the call
+    # A second call: neither torch's allocator nor the device as a whole
+    # (a cudaMalloc inside the library would show there) loses memory.
+    free_before = torch.cuda.mem_get_info()[0]
+    dsnq.block_scaled_fp8_gemm_dual_bf16a_static(a, *W, out1=o1, out2=o2)
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free_before
+    assert torch.cuda.memory_allocated() == before
     r1, r2 = dsnq.block_scaled_fp8_gemm_dual_bf16a(a, *W)
     assert torch.equal(o1, r1) and torch.equal(o2, r2)
     if M == 300:
