@@ -1155,34 +1155,43 @@ constexpr size_t smem_bytes(int KB) {
 // only.  Both CTAs' loads signal the even CTA's stage barrier
 // (TMA .cta_group::2); the MMA completions are multicast to both CTAs'
 // "stage free" and "partial ready" barriers; both CTAs' promotion warps
-// release a TMEM buffer on the even CTA's barrier.  Each promotion thread
-// carries 64 fp32 accumulators, so the role warps give up registers
-// (setmaxnreg) to the promotion warps.
+// release a TMEM buffer on the even CTA's barrier.
 //
-// A K block is issued as two column halves (MMA N=128 each) into their own
-// TMEM buffers, so the promotion of half 0 starts while the tensor core
-// works on half 1; TMEM holds two K blocks of both halves.  For an N=128
-// MMA each CTA supplies 64 weight rows, so CTA r stores weight rows
-// 128h + 64r .. +63 of the tile as chunk h of its stage.
+// A K block is four MMAs of the whole tile (M=256, N=256, K=32: 128 cycles
+// of tensor work per SM each) into one of two TMEM buffers of 256 columns;
+// each CTA supplies half of the MMA's N, CTA r storing weight rows
+// 128r .. 128r+127 of the tile.  Measured on GB300, an MMA of N=128 (64
+// cycles of work) cannot be issued faster than ~87 cycles even back to back,
+// while N=256 MMAs run at the full rate with waits in between; N=256 also
+// reads the A tile once per K slice (32 KB of shared-memory reads per K block
+// and SM, against the 32 KB the TMA writes).
+//
+// With only two buffers, the MMAs of K block g+2 wait for the promotion of
+// K block g, so promotion must read a 256-column buffer out of TMEM quickly.
+// Eight promotion warps (two per TMEM lane quarter, 128 columns each) get most
+// of the registers (setmaxnreg: 232 per thread, the role warps 40): 128 fp32
+// accumulators plus a 64-column TMEM load per thread.
 namespace pair {
-constexpr int kBN = 256;                        // output columns of a tile (both CTAs)
-constexpr int kHalfN = 128;                     // MMA N of one column half
+constexpr int kBN = 256;                        // output columns of a tile (both CTAs), the MMA's N
+constexpr int kHalfN = 128;                     // weight rows each CTA supplies (half of the MMA's N)
 constexpr int kStages = 4;
-constexpr int kNBuf = 2;                        // K blocks in TMEM (x 2 halves of 128 columns)
-constexpr int kEpiWarps = 16;
+constexpr int kNBuf = 2;                        // K blocks in TMEM (256 columns each)
+constexpr int kEpiWarps = 8;                    // two per TMEM lane quarter
 constexpr int kThreads = (4 + kEpiWarps) * 32;
 constexpr int kHalfBytes = kPRows * kBK;        // 16 KB: 128 rows x 128 K bytes
 constexpr int kStageBytes = 2 * kHalfBytes;     // this CTA's activation rows + weight rows
-constexpr int kCols = 64;                       // accumulator columns per promotion thread
-constexpr int kLdCols = 16;                     // columns per TMEM load
-constexpr int kStageOutBytes = 32 * kCols * 2;  // a promotion warp's 32 x 64 bf16 block
+constexpr int kCols = kBN / (kEpiWarps / 4);    // accumulator columns per promotion thread (128)
+constexpr int kLdCols = 64;                     // columns per TMEM load
+constexpr int kOutBlock = 64;                   // columns per output store box (128-byte rows)
+constexpr int kStageOutBytes = 32 * kCols * 2;  // a promotion warp's 32 x 128 bf16 block
 constexpr int kTmemCols = 512;
-constexpr uint32_t kRegsLaunch = 96;            // 65536 / 640, in steps of 8
-constexpr uint32_t kRegsRole = 64;
-constexpr uint32_t kRegsEpi = 104;
+constexpr uint32_t kRegsLaunch = 168;           // 65536 / 384, in steps of 8
+constexpr uint32_t kRegsRole = 40;
+constexpr uint32_t kRegsEpi = 232;
 static_assert(4 * 32 * kRegsRole + kEpiWarps * 32 * kRegsEpi <= kThreads * kRegsLaunch,
               "the register split must fit in what the block is launched with");
 static_assert(kNBuf * kBN <= kTmemCols, "TMEM holds 512 fp32 columns");
+static_assert(kCols % kLdCols == 0 && kCols % kOutBlock == 0, "whole loads and store boxes per thread");
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;
@@ -1253,14 +1262,14 @@ __device__ __forceinline__ void tc_commit_pair_local(uint32_t bar) {
         "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
         : "memory");
 }
-// Instruction descriptor: D fp32, A and B E4M3, K-major, M = 256, N = 128.
+// Instruction descriptor: D fp32, A and B E4M3, K-major, M = 256, N = 256.
 __host__ __device__ constexpr uint32_t idesc_e4m3_pair() {
-    return (1u << 4) | (static_cast<uint32_t>(kHalfN >> 3) << 17) | (static_cast<uint32_t>(256 >> 4) << 24);
+    return (1u << 4) | (static_cast<uint32_t>(kBN >> 3) << 17) | (static_cast<uint32_t>(256 >> 4) << 24);
 }
 
 constexpr size_t smem_bytes(int KB) {
     const int KBP = (KB + 3) & ~3;
-    return 1024 + kStages * kStageBytes + kEpiWarps * kStageOutBytes + (2 * kStages + 4 * kNBuf + 5) * 8 + 32 +
+    return 1024 + kStages * kStageBytes + kEpiWarps * kStageOutBytes + (2 * kStages + 2 * kNBuf + 5) * 8 + 32 +
            static_cast<size_t>(2 * KBP * kPRows + 2 * 2 * KBP) * 4;
 }
 }  // namespace pair
@@ -1277,9 +1286,9 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
     uint64_t* bars = reinterpret_cast<uint64_t*>(out_stage + kEpiWarps * kStageOutBytes);
     uint64_t* full = bars;                    // [S]  even CTA: both CTAs' loads of a stage
     uint64_t* empty = bars + kStages;         // [S]  MMA -> TMA (multicast to both)
-    uint64_t* tfull = bars + 2 * kStages;     // [2 halves][NB] MMA -> promotion (multicast to both)
-    uint64_t* tempty = tfull + 2 * kNBuf;     // [2 halves][NB] even CTA: both CTAs' promotion -> MMA
-    uint64_t* sfull = tempty + 2 * kNBuf;     // [2]
+    uint64_t* tfull = bars + 2 * kStages;     // [NB] MMA -> promotion (multicast to both)
+    uint64_t* tempty = tfull + kNBuf;         // [NB] even CTA: both CTAs' promotion -> MMA
+    uint64_t* sfull = tempty + kNBuf;         // [2]
     uint64_t* sempty = sfull + 2;             // [2]
     uint64_t* drain = sempty + 2;             // [1]
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
@@ -1309,9 +1318,9 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
             mbar_init(smem_u32(&full[s]), 1);
             mbar_init(smem_u32(&empty[s]), 1);
         }
-        for (int b = 0; b < 2 * kNBuf; ++b) {
+        for (int b = 0; b < kNBuf; ++b) {
             mbar_init(smem_u32(&tfull[b]), 1);
-            mbar_init(smem_u32(&tempty[b]), kEpiWarps);   // the 8 warps of a half, in both CTAs
+            mbar_init(smem_u32(&tempty[b]), 2 * kEpiWarps);   // every promotion warp of both CTAs
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(&sfull[i]), 32);
@@ -1347,11 +1356,11 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
     if (warp < 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsRole));
     if (warp == 0) {
-        // ------------------------------------------------ TMA producer (3*S lanes, both CTAs)
-        if (lane < 3 * kStages) {
+        // ------------------------------------------------ TMA producer (2*S lanes, both CTAs)
+        if (lane < 2 * kStages) {
             const uint32_t ng = static_cast<uint32_t>(items) * KB;
-            const int s = lane / 3;
-            const int part = lane % 3;           // 0: activation rows, 1/2: weight chunk 0/1
+            const int s = lane >> 1;
+            const int part = lane & 1;           // 0: activation rows, 1: weight rows
             const uint32_t fb = peer_addr(smem_u32(&full[s]), 0);   // the even CTA's stage barrier
             uint8_t* st = tiles + s * kStageBytes;
             uint32_t last = 0;
@@ -1382,9 +1391,8 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
                     if (even) mbar_arrive_expect_tx(smem_u32(&full[s]), 2 * kStageBytes);
                     tma_load_2d_pair(smem_u32(st), &map_a, fb, kbi * kBK, m0);
                 } else {
-                    const int h = part - 1;
-                    tma_load_2d_pair(smem_u32(st + kHalfBytes + h * (kHalfBytes / 2)), pi ? &map_w1 : &map_w0, fb,
-                                     kbi * kBK, n0 + h * kHalfN + static_cast<int>(rank) * (kHalfN / 2));
+                    tma_load_2d_pair(smem_u32(st + kHalfBytes), pi ? &map_w1 : &map_w0, fb, kbi * kBK,
+                                     n0 + static_cast<int>(rank) * kHalfN);
                 }
                 last = g + 1;
             }
@@ -1418,26 +1426,21 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
                     const int s = g % kStages;
                     const int q = g % kNBuf;
                     const uint64_t so = static_cast<uint64_t>((s * kStageBytes) >> 4);
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        if ((h == 0 && !wait_bounded<true>(smem_u32(&full[s]), (g / kStages) & 1, abort_flag, tmo)) ||
-                            !wait_bounded<true>(smem_u32(&tempty[h * kNBuf + q]), ((g / kNBuf) & 1) ^ 1, abort_flag,
-                                                tmo)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        const uint32_t d = tmem_base + static_cast<uint32_t>((2 * h + q) * kHalfN);
-                        const uint64_t wo = so + static_cast<uint64_t>((h * (kHalfBytes / 2)) >> 4);
-#pragma unroll
-                        for (int k = 0; k < kBK / kUmmaK; ++k) {
-                            const uint64_t ko = static_cast<uint64_t>((k * kUmmaK) >> 4);
-                            tc_mma_f8_pair(d, da0 + so + ko, dw0 + wo + ko, idesc, k > 0 ? 1u : 0u);
-                        }
-                        if (h == 1) tc_commit_pair_both(smem_u32(&empty[s]));
-                        tc_commit_pair_both(smem_u32(&tfull[h * kNBuf + q]));
-                        any = true;
+                    if (!wait_bounded<true>(smem_u32(&full[s]), (g / kStages) & 1, abort_flag, tmo) ||
+                        !wait_bounded<true>(smem_u32(&tempty[q]), ((g / kNBuf) & 1) ^ 1, abort_flag, tmo)) {
+                        ok = false;
+                        break;
                     }
+                    tc_fence_after();
+                    const uint32_t d = tmem_base + static_cast<uint32_t>(q * kBN);
+#pragma unroll
+                    for (int k = 0; k < kBK / kUmmaK; ++k) {
+                        const uint64_t ko = static_cast<uint64_t>((k * kUmmaK) >> 4);
+                        tc_mma_f8_pair(d, da0 + so + ko, dw0 + so + ko, idesc, k > 0 ? 1u : 0u);
+                    }
+                    tc_commit_pair_both(smem_u32(&empty[s]));    // stage free once these MMAs have read it
+                    tc_commit_pair_both(smem_u32(&tfull[q]));    // partial sum ready (both CTAs)
+                    any = true;
                 }
             }
             if (*abort_flag && any) {
@@ -1497,14 +1500,13 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
         // ------------------------------------------------ promotion + store (both CTAs)
         const int ew = warp - 4;
         const int quarter = warp & 3;            // TMEM lanes 32*quarter .. +31
-        const int slice = ew >> 2;               // columns 64*slice .. +63 of the tile
+        const int slice = ew >> 2;               // columns kCols*slice .. +kCols-1 of the tile
         const int row = quarter * 32 + lane;
         const int col0 = slice * kCols;
-        static_assert(kNBuf == 2, "two buffer-free barriers per half in the even CTA");
-        const int half = slice >> 1;             // column half of the tile (its own MMA and buffers)
-        const int hcol = (slice & 1) * kCols;    // columns within the half
-        const uint32_t tempty_even0 = peer_addr(smem_u32(&tempty[half * kNBuf + 0]), 0);
-        const uint32_t tempty_even1 = peer_addr(smem_u32(&tempty[half * kNBuf + 1]), 0);
+        static_assert(kNBuf == 2, "two buffer-free barriers in the even CTA");
+        static_assert(kCols == kPRows, "a promotion thread's columns share one weight-scale block");
+        const uint32_t tempty_even0 = peer_addr(smem_u32(&tempty[0]), 0);
+        const uint32_t tempty_even1 = peer_addr(smem_u32(&tempty[1]), 0);
         uint32_t g = 0;
         bool ok = true;
         for (int i = 0; i < items && ok; ++i) {
@@ -1517,7 +1519,7 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
                 if (!__all_sync(0xffffffffu, got)) break;
             }
             const float* sa_t = sa_slots + slot * KBP * kPRows + row;
-            const float* sw_t = sw_slots + (slot * 2 + (slice >> 1)) * KBP;
+            const float* sw_t = sw_slots + (slot * 2 + slice) * KBP;
 
             float2 acc[kCols / 2];
 #pragma unroll
@@ -1531,75 +1533,77 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
                     w_nxt = sw_t[kb + 1];
                 }
                 const int b = g % kNBuf;
-                const bool got = wait_bounded<true>(smem_u32(&tfull[half * kNBuf + b]), (g / kNBuf) & 1, abort_flag, tmo);
+                const bool got = wait_bounded<true>(smem_u32(&tfull[b]), (g / kNBuf) & 1, abort_flag, tmo);
                 if (!__all_sync(0xffffffffu, got)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 const float2 s2 = make_float2(sk, sk);
-                if (!bounds_ok((2 * half + b) * kHalfN + hcol + kCols <= kTmemCols)) {
+                if (!bounds_ok(b * kBN + col0 + kCols <= kTmemCols)) {
                     ok = false;
                     break;
                 }
                 const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
-                                       static_cast<uint32_t>((2 * half + b) * kHalfN + hcol);
-                // Four 16-column loads, each issued while the previous chunk is
-                // added in; the buffer is released as soon as the last load has
-                // completed, before its chunk is added.
-                static_assert(kCols == 4 * kLdCols && kLdCols == 16, "four 16-column chunks");
-                uint32_t ra[16], rb[16];
-                auto add = [&](int h, const uint32_t (&r)[16]) {
+                                       static_cast<uint32_t>(b * kBN + col0);
+                // The thread's columns in 64-column loads, each added in before the
+                // next is read; the buffer is released once the last load has
+                // completed, before its columns are added.
 #pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        acc[h * 8 + j] = __ffma2_rn(make_float2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1])),
-                                                    s2, acc[h * 8 + j]);
-                };
-                tmem_ld16_issue(tbase, ra);
-                tmem_ld16_wait(ra);
-                tmem_ld16_issue(tbase + 16, rb);
-                add(0, ra);
-                tmem_ld16_wait(rb);
-                tmem_ld16_issue(tbase + 32, ra);
-                add(1, rb);
-                tmem_ld16_wait(ra);
-                tmem_ld16_issue(tbase + 48, rb);
-                add(2, ra);
-                tmem_ld16_wait(rb);
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) {
-                    if (even)
-                        mbar_arrive(smem_u32(&tempty[half * kNBuf + b]));
-                    else
-                        mbar_arrive_remote(b ? tempty_even1 : tempty_even0);
+                for (int c = 0; c < kCols / kLdCols; ++c) {
+                    uint64_t r[kLdCols / 2];
+                    tmem_ld_pairs<kLdCols>(tbase + c * kLdCols, r);
+                    if (c == kCols / kLdCols - 1) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) {
+                            if (even)
+                                mbar_arrive(smem_u32(&tempty[b]));
+                            else
+                                mbar_arrive_remote(b ? tempty_even1 : tempty_even0);
+                        }
+                    }
+#pragma unroll
+                    for (int j = 0; j < kLdCols / 2; ++j)
+                        acc[c * (kLdCols / 2) + j] = __ffma2_rn(as_float2(r[j]), s2, acc[c * (kLdCols / 2) + j]);
                 }
-                add(3, rb);
                 ++g;
             }
             if (!ok) break;
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&sempty[slot]));
 
-            // Epilogue: this warp's 32 rows x 64 columns as bf16 into its
-            // staging buffer (128-byte rows, 128-byte swizzle: 16-byte chunk c
-            // of row r at chunk c ^ (r & 7)), then one TMA store.
+            // Epilogue: this warp's 32 rows x kCols columns as bf16 into its
+            // staging buffer, as blocks of 64 columns (128-byte rows, 128-byte
+            // swizzle: 16-byte chunk c of row r at chunk c ^ (r & 7)), then one
+            // TMA store per block.
             if (m0 + quarter * 32 < p.M && n0 + col0 < pr.N) {
                 uint8_t* stg = out_stage + ew * kStageOutBytes;
-                if (lane == 0) bulk_wait_read_all();   // the previous tile's store has read the buffer
+                if (lane == 0) bulk_wait_read_all();   // the previous tile's stores have read the buffer
                 __syncwarp();
 #pragma unroll
-                for (int c = 0; c < kCols / 8; ++c) {
-                    uint4 v;
-                    __nv_bfloat162* hv = reinterpret_cast<__nv_bfloat162*>(&v);
+                for (int ob = 0; ob < kCols / kOutBlock; ++ob) {
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) hv[q] = __floats2bfloat162_rn(acc[4 * c + q].x, acc[4 * c + q].y);
-                    *reinterpret_cast<uint4*>(stg + lane * (kCols * 2) + ((c ^ (lane & 7)) * 16)) = v;
+                    for (int c = 0; c < kOutBlock / 8; ++c) {
+                        uint4 v;
+                        __nv_bfloat162* hv = reinterpret_cast<__nv_bfloat162*>(&v);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const float2 f = acc[ob * (kOutBlock / 2) + 4 * c + q];
+                            hv[q] = __floats2bfloat162_rn(f.x, f.y);
+                        }
+                        *reinterpret_cast<uint4*>(stg + ob * (32 * kOutBlock * 2) + lane * (kOutBlock * 2) +
+                                                  ((c ^ (lane & 7)) * 16)) = v;
+                    }
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
-                    tma_store_2d(pi ? &map_o1 : &map_o0, smem_u32(stg), n0 + col0, m0 + quarter * 32);
+#pragma unroll
+                    for (int ob = 0; ob < kCols / kOutBlock; ++ob)
+                        if (n0 + col0 + ob * kOutBlock < pr.N)
+                            tma_store_2d(pi ? &map_o1 : &map_o0, smem_u32(stg + ob * (32 * kOutBlock * 2)),
+                                         n0 + col0 + ob * kOutBlock, m0 + quarter * 32);
                     bulk_commit();
                 }
             }
@@ -1960,9 +1964,9 @@ dsnq_status run_gemm(int64_t M, int64_t K, const void* a, int64_t lda, const flo
     const bool paired = variant == kVarPair;
     const int bn = swap ? (variant == kVarDecode32 ? 32 : variant == kVarDecode64 ? 64 : 16) : 128;
     const int a_box = swap ? bn : gemm::kPRows;
-    // The CTA-pair kernel loads weight rows in chunks of 64 (each CTA's share
-    // of an N=128 MMA).
-    const int w_box = swap ? gemm::kPRows : (paired ? gemm::pair::kHalfN / 2 : bn);
+    // The CTA-pair kernel loads each CTA's 128 weight rows of a tile (its half
+    // of the MMA's N=256) as one box.
+    const int w_box = swap ? gemm::kPRows : (paired ? gemm::pair::kHalfN : bn);
 
     gemm::Params prm{};
     prm.M = static_cast<int>(M);
