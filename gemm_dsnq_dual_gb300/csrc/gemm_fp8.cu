@@ -23,7 +23,8 @@
 //     (tcgen05.ld), multiply by sa * sw and add it into fp32 registers while
 //     the MMAs of the next K blocks fill the other buffers.
 //   * Warp roles: warp 0 issues TMA, warp 1 allocates TMEM and issues MMA
-//     (the whole warp runs the loop, one elected lane issues), warp 2 idles,
+//     (the whole warp runs the loop, one elected lane issues), warp 2 idles
+//     (in the CTA-pair kernel it issues the output stores),
 //     warp 3 loads the scales, warps 4.. promote and store.  The MMA warp
 //     itself waits for "stage loaded" and "TMEM buffer free".  A separate gate
 //     thread that waited on those and published a count of ready K blocks
@@ -1168,9 +1169,14 @@ constexpr size_t smem_bytes(int KB) {
 //
 // With only two buffers, the MMAs of K block g+2 wait for the promotion of
 // K block g, so promotion must read a 256-column buffer out of TMEM quickly.
-// Eight promotion warps (two per TMEM lane quarter, 128 columns each) get most
-// of the registers (setmaxnreg: 232 per thread, the role warps 40): 128 fp32
-// accumulators plus a 64-column TMEM load per thread.
+// Eight promotion warps (two per TMEM lane quarter, 128 columns each) hold
+// 128 fp32 accumulators plus a 64-column TMEM load per thread (the compiler
+// allocates the launch's 168 registers per thread; setmaxnreg moves the role
+// warps' share to the promotion warps at run time).  Warp 2 issues the output
+// stores, so that a promotion warp's epilogue is only its conversion and
+// shared-memory writes: with the stores issued by the promotion warps
+// themselves (they wait behind the operand loads in the TMA queue) the kernel
+// took 330 instead of 308 us at M=8192.
 namespace pair {
 constexpr int kBN = 256;                        // output columns of a tile (both CTAs), the MMA's N
 constexpr int kHalfN = 128;                     // weight rows each CTA supplies (half of the MMA's N)
@@ -1269,7 +1275,7 @@ __host__ __device__ constexpr uint32_t idesc_e4m3_pair() {
 
 constexpr size_t smem_bytes(int KB) {
     const int KBP = (KB + 3) & ~3;
-    return 1024 + kStages * kStageBytes + kEpiWarps * kStageOutBytes + (2 * kStages + 2 * kNBuf + 5) * 8 + 32 +
+    return 1024 + kStages * kStageBytes + kEpiWarps * kStageOutBytes + (2 * kStages + 2 * kNBuf + 7) * 8 + 32 +
            static_cast<size_t>(2 * KBP * kPRows + 2 * 2 * KBP) * 4;
 }
 }  // namespace pair
@@ -1291,7 +1297,9 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
     uint64_t* sfull = tempty + kNBuf;         // [2]
     uint64_t* sempty = sfull + 2;             // [2]
     uint64_t* drain = sempty + 2;             // [1]
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+    uint64_t* ofull = drain + 1;              // [1]  promotion warps -> store warp: staging written
+    uint64_t* ofree = ofull + 1;              // [1]  store warp -> promotion warps: staging read by the stores
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(ofree + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
     const int KBP = (p.KB + 3) & ~3;
     float* sa_slots = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(tmem_holder + 8) + 15) & ~uintptr_t(15));
@@ -1327,6 +1335,8 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
             mbar_init(smem_u32(&sempty[i]), kEpiWarps);
         }
         mbar_init(smem_u32(drain), 1);
+        mbar_init(smem_u32(ofull), kEpiWarps);
+        mbar_init(smem_u32(ofree), 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         tma_prefetch_desc(&map_a);
@@ -1447,6 +1457,35 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
                 tc_commit_pair_local(smem_u32(drain));
                 wait_drain(smem_u32(drain), 0, tmo);
             }
+        }
+        __syncwarp();
+    } else if (warp == 2) {
+        // ------------------------------------------------ output stores (lane 0, both CTAs)
+        // The promotion warps write a tile's bf16 blocks into their staging
+        // buffers; this warp issues the TMA stores and hands the buffers back
+        // once the stores have read them, so that issuing the stores (which
+        // waits behind the operand loads in the TMA queue) stays off the
+        // promotion warps' path.
+        if (lane == 0) {
+            for (int i = 0; i < items; ++i) {
+                if (!wait_bounded(smem_u32(ofull), i & 1, abort_flag, tmo)) break;
+                int pi, m0, n0;
+                coords(first + i * stride, pi, m0, n0);
+                const Problem pr = pi ? p.prob[1] : p.prob[0];
+                for (int ew = 0; ew < kEpiWarps; ++ew) {
+                    const int quarter = (ew + 4) & 3, col0 = (ew >> 2) * kCols;
+                    if (m0 + quarter * 32 >= p.M || n0 + col0 >= pr.N) continue;
+                    uint8_t* stg = out_stage + ew * kStageOutBytes;
+                    for (int ob = 0; ob < kCols / kOutBlock; ++ob)
+                        if (n0 + col0 + ob * kOutBlock < pr.N)
+                            tma_store_2d(pi ? &map_o1 : &map_o0, smem_u32(stg + ob * (32 * kOutBlock * 2)),
+                                         n0 + col0 + ob * kOutBlock, m0 + quarter * 32);
+                }
+                bulk_commit();
+                bulk_wait_read_all();            // the stores have read the staging buffers
+                mbar_arrive(smem_u32(ofree));
+            }
+            bulk_wait_all();                     // every store has completed before the CTA exits
         }
         __syncwarp();
     } else if (warp == 3) {
@@ -1575,12 +1614,15 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
 
             // Epilogue: this warp's 32 rows x kCols columns as bf16 into its
             // staging buffer, as blocks of 64 columns (128-byte rows, 128-byte
-            // swizzle: 16-byte chunk c of row r at chunk c ^ (r & 7)), then one
-            // TMA store per block.
+            // swizzle: 16-byte chunk c of row r at chunk c ^ (r & 7)); warp 2
+            // issues the TMA stores.  Every promotion warp signals every tile
+            // (the store warp counts them), whether or not its block is in range.
+            if (i > 0) {
+                const bool got = wait_bounded(smem_u32(ofree), (i - 1) & 1, abort_flag, tmo);
+                if (!__all_sync(0xffffffffu, got)) break;
+            }
             if (m0 + quarter * 32 < p.M && n0 + col0 < pr.N) {
                 uint8_t* stg = out_stage + ew * kStageOutBytes;
-                if (lane == 0) bulk_wait_read_all();   // the previous tile's stores have read the buffer
-                __syncwarp();
 #pragma unroll
                 for (int ob = 0; ob < kCols / kOutBlock; ++ob) {
 #pragma unroll
@@ -1597,20 +1639,12 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constan
                     }
                 }
                 fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-#pragma unroll
-                    for (int ob = 0; ob < kCols / kOutBlock; ++ob)
-                        if (n0 + col0 + ob * kOutBlock < pr.N)
-                            tma_store_2d(pi ? &map_o1 : &map_o0, smem_u32(stg + ob * (32 * kOutBlock * 2)),
-                                         n0 + col0 + ob * kOutBlock, m0 + quarter * 32);
-                    bulk_commit();
-                }
             }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(ofull));
         }
     }
 
-    if (warp >= 4 && lane == 0) bulk_wait_all();
     tc_fence_before();
     __syncthreads();
     cluster_sync_all();          // no CTA leaves while its peer may still address its memory
