@@ -29,6 +29,8 @@
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 #include "debug_check.cuh"
 #include "dsnq_internal.h"
 #include "group_quant.cuh"
@@ -390,9 +392,17 @@ warp_row_kernel(const RowArgs a) {
 // columns, one 128-column group per half-warp and slot) and Kkv = 512 (2
 // slots).  Lane l holds chunks l, l+32, ... of the row (16 bytes each).
 //   * each slot's role is known at compile time (no per-chunk predicates);
-//   * the next row of the warp is loaded into registers as soon as the
-//     current one is unpacked (an L2 prefetch of the row after that, on top,
-//     measured slower: M=32768 42.2 vs 40.2 us);
+//   * rows reach the warp through a ring of kRingRows row buffers in shared
+//     memory that its lanes fill with cp.async: the warp's first kRingRows
+//     rows are requested at once, and each row read out of the ring is
+//     replaced by the request for the row kRingRows further on, so the loads
+//     run ahead of the arithmetic by that many rows without holding
+//     registers.  Each lane copies and later reads only its own chunks, so
+//     its own cp.async.wait_group orders the two.  Measured on GB300 against
+//     the next row held in registers (four-warp CTAs, four per SM): M=2048
+//     6.65 -> 6.02 us, M=8192 14.7-15.0 -> 14.5 us, M=32768 40.2 -> 39.2 us
+//     per call in a graph; three rows in flight, 16-warp CTAs, or three
+//     CTAs per SM (80 registers, spills) measured slower;
 //   * the work that is the same for a whole warp is done once, by the lanes
 //     it concerns, and handed to the others by shuffles:
 //       - the two sums of squares are reduced by a reduce-scatter (lanes
@@ -406,10 +416,25 @@ warp_row_kernel(const RowArgs a) {
 //   * the quantize step uses bracket reciprocals scaled once per group and
 //     takes the exactness decision for three slots with one warp vote.
 // ---------------------------------------------------------------------------
-constexpr int kFusedCtasPerSM = 4;  // register budget: 128 per thread
+constexpr int kFusedWarps = 8;      // warps (rows in work) per CTA
+constexpr int kFusedCtasPerSM = 2;  // register budget: 128 per thread
+constexpr int kRingRows = 2;        // rows in flight per warp
+constexpr int kDsv4RowBytes = (6 + 2) * 256 * 2;   // one q + kv row in bf16 (4 KB)
+
+__host__ __device__ constexpr size_t fused_smem_bytes() {
+    return static_cast<size_t>(8 * 256) * sizeof(float) +
+           static_cast<size_t>(kFusedWarps) * kRingRows * kDsv4RowBytes;
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 template <int QS, int KS>
-__global__ void __launch_bounds__(kRowWarps * 32, kFusedCtasPerSM)
+__global__ void __launch_bounds__(kFusedWarps * 32, kFusedCtasPerSM)
 warp_row_fused_kernel(const RowArgs a) {
     static_assert(QS == 6 && KS == 2, "the lane roles below are laid out for the DSv4 row");
     grid_dependency_wait();      // inputs are read only once the previous kernel's writes are visible
@@ -417,31 +442,39 @@ warp_row_fused_kernel(const RowArgs a) {
     bounds_self_test(a.inject);
     constexpr int CPT = QS + KS;
     constexpr unsigned kAll = 0xffffffffu;
-    extern __shared__ float gamma_s[];          // [(QS + KS) * 256] fp32: gamma_q then gamma_kv
+    extern __shared__ __align__(16) float gamma_s[];   // [(QS + KS) * 256] fp32: gamma_q then gamma_kv; then the rings
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     constexpr int kq = QS * 256, width = CPT * 256;
+    static_assert(CPT * 256 * 2 == kDsv4RowBytes, "ring slots hold one row");
     const bool q_half = lane < 16;              // reduce-scatter roles
     const bool hi8 = (lane & 8) != 0;
     const int gi = lane & 7;                    // group slot this lane forms (when < 3)
     const int h = lane >> 4;                    // half-warp: group 2j + h in slot j
+    // This lane's 16-byte chunk of slot j of ring row r: byte r * row + j * 512 + lane * 16.
+    const uint32_t ring = static_cast<uint32_t>(__cvta_generic_to_shared(gamma_s + width)) +
+                          static_cast<uint32_t>(warp * kRingRows * kDsv4RowBytes + lane * 16);
 
-    auto load_row = [&](int64_t m, uint4 (&raw)[CPT]) {
-        const __nv_bfloat16* qrow = a.q + m * a.ldq + lane * kChunk;
-        const __nv_bfloat16* kvrow = a.kv + m * a.ldkv + lane * kChunk;
-        const bool in = bounds_ok(m < a.M && a.cq == QS * 32 && a.ckv == KS * 32);
+    // Requests row mm into ring row r (nothing past the last row); always one
+    // commit group, so that the group count stays one per ring step.
+    auto request_row = [&](int64_t mm, int r) {
+        const bool in = bounds_ok(a.cq == QS * 32 && a.ckv == KS * 32 && r < kRingRows);
+        if (mm < a.M && in) {
+            const __nv_bfloat16* qrow = a.q + mm * a.ldq + lane * kChunk;
+            const __nv_bfloat16* kvrow = a.kv + mm * a.ldkv + lane * kChunk;
 #pragma unroll
-        for (int j = 0; j < CPT; ++j)
-            raw[j] = in ? __ldg(reinterpret_cast<const uint4*>(j < QS ? qrow + j * 256 : kvrow + (j - QS) * 256))
-                        : make_uint4(0, 0, 0, 0);
+            for (int j = 0; j < CPT; ++j)
+                cp_async16(ring + r * kDsv4RowBytes + j * 512, j < QS ? qrow + j * 256 : kvrow + (j - QS) * 256);
+        }
+        cp_async_commit();
     };
 
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * kRowWarps;
-    int64_t m = static_cast<int64_t>(blockIdx.x) * kRowWarps + warp;
-    uint4 cur[CPT];
-    if (m < a.M) load_row(m, cur);               // in flight while gamma is staged
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kFusedWarps;
+    int64_t m = static_cast<int64_t>(blockIdx.x) * kFusedWarps + warp;
+#pragma unroll
+    for (int r = 0; r < kRingRows; ++r) request_row(m + r * stride, r);   // in flight while gamma is staged
 
-    for (int i = threadIdx.x * kChunk; i < width; i += kRowWarps * 32 * kChunk) {
+    for (int i = threadIdx.x * kChunk; i < width; i += kFusedWarps * 32 * kChunk) {
         const __nv_bfloat16* gsrc = i < kq ? a.gamma_q + i : a.gamma_kv + (i - kq);
         float2 g[4];
         unpack8(__ldg(reinterpret_cast<const uint4*>(gsrc)), g);
@@ -451,11 +484,25 @@ warp_row_fused_kernel(const RowArgs a) {
     __syncthreads();
 
     const float kdiv = q_half ? a.kq_f : a.kkv_f;
+    int r = 0;
     for (; m < a.M; m += stride) {
+        cp_async_wait<kRingRows - 1>();          // this lane's chunks of row m have landed
         float2 x[CPT][4];
 #pragma unroll
-        for (int j = 0; j < CPT; ++j) unpack8(cur[j], x[j]);
-        if (m + stride < a.M) load_row(m + stride, cur);   // next row, in flight meanwhile
+        for (int j = 0; j < CPT; ++j) {
+            uint4 v;
+            asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                         : "r"(ring + r * kDsv4RowBytes + j * 512)
+                         : "memory");
+            unpack8(v, x[j]);
+        }
+        // The chunks are in registers, so the ring row can take the row
+        // kRingRows steps ahead (the warp barrier orders the reads above
+        // before the copies that overwrite them).
+        __syncwarp();
+        request_row(m + kRingRows * stride, r);
+        r = r + 1 == kRingRows ? 0 : r + 1;
 
         // Sums of squares, then the reduce-scatter: lanes 0-15 finish the q
         // sum, lanes 16-31 the kv sum, each over the 32 lanes' partials.
@@ -554,6 +601,24 @@ warp_row_fused_kernel(const RowArgs a) {
                     *reinterpret_cast<uint2*>(crow + (j0 + u) * 256) = codes[u];
         }
     }
+    cp_async_wait<0>();          // no copy outstanding when the CTA exits (rows past the end request none)
+}
+
+// The staged kernel's shared memory is above the default 48 KB limit; the
+// attribute is set once per device.
+static bool fused_smem_ready() {
+    static std::mutex mu;
+    static bool done[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!done[dev]) {
+        if (cudaFuncSetAttribute(warp_row_fused_kernel<6, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(fused_smem_bytes())) != cudaSuccess)
+            return false;
+        done[dev] = true;
+    }
+    return true;
 }
 
 template <int MODE>
@@ -568,11 +633,11 @@ static dsnq_status launch_rows(RowArgs a, int64_t M, cudaStream_t s) {
     const int64_t warp_row_min = sms > 0 ? static_cast<int64_t>(sms) * 8 : 2048;
     if (MODE == kFused && a.cq == 6 * 32 && a.ckv == 2 * 32 && M >= warp_row_min) {
         // DSv4 rows (Kq = 1536, Kkv = 512): the specialized warp-per-row kernel.
-        const int64_t rows_cap = sms > 0 ? static_cast<int64_t>(sms) * kFusedCtasPerSM : (M + kRowWarps - 1) / kRowWarps;
-        const int64_t need = (M + kRowWarps - 1) / kRowWarps;
-        dim3 grid(static_cast<unsigned>(need < rows_cap ? need : rows_cap)), block(kRowWarps * 32);
-        return launch_result(launch_kernel(warp_row_fused_kernel<6, 2>, grid, block,
-                                           static_cast<size_t>(chunks) * kChunk * sizeof(float), s, a));
+        if (!fused_smem_ready()) return DSNQ_ERR_CUDA;
+        const int64_t rows_cap = sms > 0 ? static_cast<int64_t>(sms) * kFusedCtasPerSM : (M + kFusedWarps - 1) / kFusedWarps;
+        const int64_t need = (M + kFusedWarps - 1) / kFusedWarps;
+        dim3 grid(static_cast<unsigned>(need < rows_cap ? need : rows_cap)), block(kFusedWarps * 32);
+        return launch_result(launch_kernel(warp_row_fused_kernel<6, 2>, grid, block, fused_smem_bytes(), s, a));
     }
     if (chunks <= 8 * 32 && M >= warp_row_min) {
         // Warp per row.  Enough CTAs to fill every SM at the register-limited occupancy.
