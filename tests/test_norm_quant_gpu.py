@@ -184,6 +184,15 @@ def test_ragged_shapes_and_small_widths():
         check_against_oracle(lat, dsnq.ROW_MAJOR)
 
 
+@pytest.mark.parametrize("M", [1216, 1217, 3001, 4869])
+@pytest.mark.parametrize("layout", [dsnq.ROW_MAJOR, dsnq.COL_MAJOR])
+def test_warp_per_row_ragged_row_counts_split_views(M, layout):
+    """DSv4 rows at and past the warp-per-row dispatch point (8 rows per SM on
+    the 152-SM part), with row counts that leave warps with zero, one or
+    several rows and a ragged last row-round, read from strided split views."""
+    check_against_oracle(inputs.decode_batch(M, seed=M), layout)
+
+
 def test_zero_rows_enqueue_nothing():
     q = torch.empty(0, 1536, dtype=torch.bfloat16, device="cuda")
     kv = torch.empty(0, 512, dtype=torch.bfloat16, device="cuda")
