@@ -1807,9 +1807,10 @@ struct Consumer {
 
 // Every CTA quantizes all M rows itself, so the in-GEMM quantization pays
 // only while each of its ten quantizer warps has one batch of four 256-column
-// units (measured on GB300 at K=1536: M=1 12.6 us vs 14.1 us for the quant
-// kernel then the GEMM; M=16 17.3 vs 14.9 us).  At most 16 rows (MMA N=16),
-// K <= 2048.
+// units (measured on GB300 at K=1536, per call in a graph: M=1 11.1 us vs
+// 13.1-13.4 us for the quant kernel then the GEMM, M=6 12.6 vs 13.1-13.4;
+// with the bound raised, M=8 / 12 / 16 took 13.9 / 15.2 / 16.4 us against
+// 13.1-13.4).  At most 16 rows (MMA N=16), K <= 2048.
 bool bf16a_in_gemm(int64_t M, int64_t K) {
     const int64_t slots = (K / 128 + 1) / 2;
     return M >= 1 && M <= 16 && K <= 2048 && M * slots <= 40;
@@ -1857,8 +1858,8 @@ size_t variant_smem(int v, int KB) {
         case kVarTile128: return gemm::smem_bytes<128, false, 5, 4, 16>(KB);
         case kVarTile128K: return gemm::smem_bytes<128, false, 3, 4, 16>(KB);
         case kVarPair: return gemm::pair::smem_bytes(KB);
-        case kVarDecodeQuant: return gemm::smem_bytes<16, true, 8, 32, 8, 1>(KB);
-        case kVarDecodeNormQuant: return gemm::smem_bytes<16, true, 8, 32, 8, 2>(KB);
+        case kVarDecodeQuant: return gemm::smem_bytes<16, true, 5, 16, 8, 1>(KB);
+        case kVarDecodeNormQuant: return gemm::smem_bytes<16, true, 5, 16, 8, 2>(KB);
     }
     return 0;
 }
@@ -2073,8 +2074,13 @@ dsnq_status run_gemm(int64_t M, int64_t K, const void* a, int64_t lda, const flo
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     switch (variant) {
-        case kVarDecodeQuant: return launch<16, true, 8, 32, 8, 1>(prm, ma, mw[0], mw[1], mo[0], mo[1], s);
-        case kVarDecodeNormQuant: return launch<16, true, 8, 32, 8, 2>(prm, ma, mw[0], mw[1], mo[0], mo[1], s);
+        // Decode on bf16 activations quantized (and normalized) in the
+        // prologue: two CTAs per SM like the 16-token decode variant (five
+        // stages, half of TMEM each), so that all 224 weight tiles stream in
+        // one wave (M=1: 14.1 -> 11.1 us per call in a graph; with one CTA
+        // per SM, eight stages, 72 SMs took a second tile).
+        case kVarDecodeQuant: return launch<16, true, 5, 16, 8, 1, 2>(prm, ma, mw[0], mw[1], mo[0], mo[1], s);
+        case kVarDecodeNormQuant: return launch<16, true, 5, 16, 8, 2, 2>(prm, ma, mw[0], mw[1], mo[0], mo[1], s);
         case kVarPair: return launch_pair(prm, ma, mw[0], mw[1], mo[0], mo[1], s);
         // Decode: the kernel streams the weights.  Up to 32 tokens two CTAs
         // share an SM (five stages, half of TMEM each), so that all 224
