@@ -563,92 +563,102 @@ __device__ __forceinline__ void quantize_activations(const Params& p, uint8_t* a
 }
 
 // In-kernel RMSNorm + per-1x128 quantization of the decode rows (the fused
-// norm+quant of the q latent, then the GEMM, in one launch): warp qw takes
-// rows qw, qw + nw, ... whole, the row and gamma in registers, loaded in one
-// round.  The sum of squares is accumulated per lane in two fp32 pairs and
-// summed across the warp by a butterfly, r = 1/sqrt(ssq/K + eps) with IEEE
-// operations,
-// x_hat = (x * r) * gamma in fp32, then the group quant of
-// quantize_activations, four slots at a time.  CTA 0 also writes the q codes
-// and scales when asked (the kv latent: norm_kv_rows, after the operand is
-// ready).  Splitting a row over several warps measured slower: the runtime
-// slot index sends the row to local memory.
+// norm+quant of the q latent, then the GEMM, in one launch).  The live rows
+// are cut into 256-column units (one row slot: a group per half-warp) spread
+// over the nw quantizer warps, four per warp, as in quantize_activations, so
+// that one row's loads and arithmetic run on several warps at once:
+//   1. each warp loads its units' row chunks, sums the squares of each unit
+//      across the warp and leaves the sum in shared memory;
+//   2. after a barrier of the quantizer warps, each warp adds its row's unit
+//      sums in slot order, takes r = 1/sqrt(ssq/K + eps) with IEEE
+//      operations, reads the chunk again (from L1) with gamma, forms
+//      x^ = (x r) gamma and quantizes its units.
+// (The fp32 summation order differs from the norm+quant kernel's; both are
+// checked against the oracle.)  The dispatch bound (M * slots <= 40) keeps
+// every unit in one round of four per warp over the ten quantizer warps.
 template <int BN>
 __device__ __forceinline__ void norm_quantize_activations(const Params& p, uint8_t* a_res, float* sa_slots,
                                                           int slot_stride, int qw, int nw, int lane) {
+    constexpr int kU = 4;                       // units per warp
     constexpr int kMaxSlots = 8;                // 256 columns per slot: K <= 2048
-    constexpr int kU = 4;                       // slots quantized together
+    __shared__ float unit_ssq[16 * kMaxSlots];  // [row][slot], rows < 16 (MMA N = 16)
     const int KB = p.KB;
     const int live = p.M < BN ? p.M : BN;
     zero_rows<BN>(KB, live, a_res, sa_slots, slot_stride, qw, nw, lane);
     const int slots = (KB + 1) / 2;
+    const int units = live * slots;
     const int h = lane >> 4;                    // half-warp h of slot i holds group 2i + h
     const int c16 = (lane & 15) >> 1;
     const bool side = blockIdx.x == 0;
     const int K = KB * kBK;
-    for (int m = qw; m < live; m += nw) {
-        const __nv_bfloat16* row = p.a_bf16 + static_cast<int64_t>(m) * p.lda_bf16;
-        uint4 raw[kMaxSlots], graw[kMaxSlots];
+    if (!bounds_ok(units <= kU * nw && slots <= kMaxSlots && live <= 16)) return;   // (debug build) outside the dispatch bound
+
+    int row[kU], slot[kU];
+    bool on[kU], in[kU];
+    // The lane's chunk of unit j (odd KB: the last slot's second half is past
+    // the row and reads as zero).
+    auto load_unit = [&](int j) {
+        return in[j] ? __ldg(reinterpret_cast<const uint4*>(p.a_bf16 + static_cast<int64_t>(row[j]) * p.lda_bf16 +
+                                                             (slot[j] * 32 + lane) * 8))
+                     : make_uint4(0, 0, 0, 0);
+    };
+    uint4 raw[kU];
 #pragma unroll
-        for (int i = 0; i < kMaxSlots; ++i) {
-            raw[i] = graw[i] = make_uint4(0, 0, 0, 0);
-            if (i < slots && 2 * i + h < KB && bounds_ok(m < p.M && (i * 32 + lane) * 8 + 8 <= K)) {
-                raw[i] = __ldg(reinterpret_cast<const uint4*>(row + (i * 32 + lane) * 8));
-                graw[i] = __ldg(reinterpret_cast<const uint4*>(p.gamma_q + (i * 32 + lane) * 8));
-            }
-        }
-        float2 sq[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+    for (int j = 0; j < kU; ++j) {
+        const int u = qw + j * nw;
+        on[j] = u < units;
+        row[j] = on[j] ? u / slots : 0;
+        slot[j] = on[j] ? u - row[j] * slots : 0;
+        in[j] = on[j] && (slot[j] * 32 + lane) * 8 + 8 <= K && bounds_ok(row[j] < p.M);
+        raw[j] = load_unit(j);
+    }
+    // 1. The squares, summed per unit across the warp.
 #pragma unroll
-        for (int i = 0; i < kMaxSlots; ++i) {
-            if (i >= slots) break;
-            float2 x[4];
-            unpack8(raw[i], x);
+    for (int j = 0; j < kU; ++j) {
+        float2 x[4];
+        unpack8(raw[j], x);
+        float2 sq = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int t = 0; t < 4; ++t) sq[t & 1] = fma2(x[t], x[t], sq[t & 1]);
-        }
-        const float ssq = warp_sum((sq[0].x + sq[1].x) + (sq[0].y + sq[1].y));
+        for (int t = 0; t < 4; ++t) sq = fma2(x[t], x[t], sq);
+        const float s = warp_sum(sq.x + sq.y);
+        if (on[j] && lane == 0) unit_ssq[row[j] * kMaxSlots + slot[j]] = s;
+    }
+    asm volatile("bar.sync 1, %0;" ::"r"(nw * 32) : "memory");   // the quantizer warps only
+
+#pragma unroll
+    for (int j = 0; j < kU; ++j) {
+        if (!on[j]) continue;
+        float ssq = 0.f;
+        for (int i = 0; i < slots; ++i) ssq += unit_ssq[row[j] * kMaxSlots + i];
         const float r = 1.0f / sqrtf(ssq / p.kq_f + p.eps);   // correctly rounded sqrt and divide
         const float2 r2 = make_float2(r, r);
+        // The chunk again (an L1 hit: this warp read it above) and gamma.
+        const uint4 graw = in[j] ? __ldg(reinterpret_cast<const uint4*>(p.gamma_q + (slot[j] * 32 + lane) * 8))
+                                 : make_uint4(0, 0, 0, 0);
+        float2 x[4], g[4];
+        unpack8(load_unit(j), x);
+        unpack8(graw, g);
 #pragma unroll
-        for (int i0 = 0; i0 < kMaxSlots; i0 += kU) {
-            if (i0 >= slots) break;
-            float2 x[kU][4];
-            float amax[kU];
+        for (int t = 0; t < 4; ++t) x[t] = mul2(mul2(x[t], r2), g[t]);
+        float amax = fmaxf(fmaxf(fmaxf(fabsf(x[0].x), fabsf(x[0].y)), fmaxf(fabsf(x[1].x), fabsf(x[1].y))),
+                           fmaxf(fmaxf(fabsf(x[2].x), fabsf(x[2].y)), fmaxf(fabsf(x[3].x), fabsf(x[3].y))));
 #pragma unroll
-            for (int j = 0; j < kU; ++j) {
-                float2 g[4];
-                unpack8(raw[i0 + j], x[j]);
-                unpack8(graw[i0 + j], g);
-#pragma unroll
-                for (int t = 0; t < 4; ++t) x[j][t] = mul2(mul2(x[j][t], r2), g[t]);
-                amax[j] = fmaxf(fmaxf(fmaxf(fabsf(x[j][0].x), fabsf(x[j][0].y)), fmaxf(fabsf(x[j][1].x), fabsf(x[j][1].y))),
-                                fmaxf(fmaxf(fabsf(x[j][2].x), fabsf(x[j][2].y)), fmaxf(fabsf(x[j][3].x), fabsf(x[j][3].y))));
-            }
-#pragma unroll
-            for (int o = 8; o > 0; o >>= 1) {
-#pragma unroll
-                for (int j = 0; j < kU; ++j) amax[j] = fmaxf(amax[j], __shfl_xor_sync(0xffffffffu, amax[j], o));
-            }
-#pragma unroll
-            for (int j = 0; j < kU; ++j) {
-                const int i = i0 + j, kb = 2 * i + h;
-                if (i >= slots || kb >= KB) continue;
-                if (!bounds_ok(m < BN && m < p.M && kb * BN + m < slot_stride)) continue;
-                const GroupQuant gq = make_group_quant(amax[j]);
-                bool ok;
-                uint2 codes = quant8_bracket(x[j], gq, ok);
-                if (!ok) codes = quant8_divide(x[j], gq.scale);
-                *reinterpret_cast<uint2*>(a_res + kb * (BN * kBK) + m * kBK + ((c16 ^ (m & 7)) << 4) + (lane & 1) * 8) =
-                    codes;
-                if ((lane & 15) == 0) {
-                    sa_slots[kb * BN + m] = gq.scale;
-                    sa_slots[slot_stride + kb * BN + m] = gq.scale;
-                }
-                if (side && p.q_out && bounds_ok((i * 32 + lane) * 8 + 8 <= K))
-                    *reinterpret_cast<uint2*>(p.q_out + static_cast<int64_t>(m) * K + (i * 32 + lane) * 8) = codes;
-                if (side && p.qs_out && (lane & 15) == 0) p.qs_out[static_cast<int64_t>(kb) * p.M + m] = gq.scale;
-            }
+        for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        const int m = row[j], kb = 2 * slot[j] + h;
+        if (kb >= KB) continue;                 // odd KB: past the row (this half-warp only; no shuffles follow)
+        if (!bounds_ok(m < BN && m < p.M && kb * BN + m < slot_stride)) continue;
+        const GroupQuant gq = make_group_quant(amax);
+        bool ok;
+        uint2 codes = quant8_bracket(x, gq, ok);
+        if (!ok) codes = quant8_divide(x, gq.scale);
+        *reinterpret_cast<uint2*>(a_res + kb * (BN * kBK) + m * kBK + ((c16 ^ (m & 7)) << 4) + (lane & 1) * 8) = codes;
+        if ((lane & 15) == 0) {
+            sa_slots[kb * BN + m] = gq.scale;
+            sa_slots[slot_stride + kb * BN + m] = gq.scale;
         }
+        if (side && p.q_out && bounds_ok((slot[j] * 32 + lane) * 8 + 8 <= K))
+            *reinterpret_cast<uint2*>(p.q_out + static_cast<int64_t>(m) * K + (slot[j] * 32 + lane) * 8) = codes;
+        if (side && p.qs_out && (lane & 15) == 0) p.qs_out[static_cast<int64_t>(kb) * p.M + m] = gq.scale;
     }
 }
 
