@@ -301,7 +301,10 @@ def headline(line: dict) -> dict:
     h["norm_quant_speedup_vs_unfused"] = {m: v.get("speedup_vs_unfused") for m, v in sw.items() if isinstance(v, dict)}
     h["norm_quant_step_frac_hbm_M8192"] = line["roofline_norm_quant"]["frac"]
     if "decode_step_us_at_M1" in line:
-        h["decode_step_us_at_M1"] = line["decode_step_us_at_M1"].get("overlap")
+        ds1 = line["decode_step_us_at_M1"]
+        h["decode_step_us_at_M1"] = ds1.get("overlap")
+        if ds1.get("one_launch") is not None:
+            h["decode_step_us_at_M1_one_launch"] = ds1["one_launch"]
     gs = line.get("gemm_sweep", {})
     if "1" in gs:
         h["gemm_dual_M1_graph_us"] = gs["1"].get("graph_us")

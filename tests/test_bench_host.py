@@ -69,7 +69,7 @@ def test_headline_keeps_the_metric_numbers():
     line = {"roofline": {"achieved": 2000.0, "frac": 0.51}, "roofline_norm_quant": {"frac": 0.4},
             "norm_quant_us_at_M1": 2.4,
             "norm_quant_sweep": {"8192": {"fused_graph_frac_hbm": 0.52, "speedup_vs_unfused": 2.5}, "note": "x"},
-            "decode_step_us_at_M1": {"overlap": 13.0},
+            "decode_step_us_at_M1": {"overlap": 13.0, "one_launch": 12.3},
             "gemm_sweep": {"1": {"graph_us": 10.8, "graph_frac_hbm": 0.6}, "1024": {"tflops": 1600.0},
                            "32768_long_context_attn": {"tflops": 2000.0, "frac_fp8": 0.52}},
             "decode_sweep": {"1": {"row_us": 2.5, "col_us": 2.5}, "note": "x"},
@@ -79,6 +79,7 @@ def test_headline_keeps_the_metric_numbers():
     assert h["norm_quant_graph_frac_hbm"] == {"8192": 0.52}
     assert h["gemm_attn_M32768_frac_fp8"] == 0.52 and h["gemm_dual_M8192_frac_fp8"] == 0.51
     assert h["norm_quant_decode_us"] == {"1": [2.5, 2.5]}
+    assert h["decode_step_us_at_M1"] == 13.0 and h["decode_step_us_at_M1_one_launch"] == 12.3
     assert h["cpu_oracle_tflops"] == {"cores": 16, "all": 0.1, "one_thread": 0.02}
 
 
