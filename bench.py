@@ -637,6 +637,14 @@ def e2e_measurement(torch, dsnq, lat, dev, weights, args, M):
     z.record(s_in)
     torch.cuda.synchronize(dev)
     ms = a.elapsed_time(z) / reps
+    # Every step copies out the same products: the host buffers must hold
+    # exactly those of a plain call (a race between the streams would not).
+    q8, s8, kvo = dsnq.fused_dual_rmsnorm_group_quant(q_h.to(dev), kv_h.to(dev), gq, gkv, lat.eps, scale_layout="col")
+    ra, ri = dsnq.block_scaled_fp8_gemm_dual(q8, s8, wa, swa, wi, swi)
+    torch.cuda.synchronize(dev)
+    for host, want in ((oa_h, ra), (oi_h, ri), (kvo_h, kvo)):
+        if not torch.equal(host.view(torch.int16), want.view(torch.int16).cpu()):
+            raise RuntimeError("e2e: the outputs copied out by the pipelined steps differ from a plain call")
     h2d = q_h.numel() * 2 + kv_h.numel() * 2
     d2h = (oa_h.numel() + oi_h.numel() + kvo_h.numel()) * 2
     return {"value": round(gemm_flops(M) / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
