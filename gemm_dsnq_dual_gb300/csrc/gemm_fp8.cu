@@ -811,6 +811,10 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                 tma_prefetch_l2(pi ? &map_w1 : &map_w0, kb * kBK, n0);
         }
     }
+    // The producer's first tile, worked out before the dependency wait (it
+    // reads only the launch parameters).
+    int pre_pi = 0, pre_m0 = 0, pre_n0 = 0;
+    if (warp == 0 && static_cast<int>(blockIdx.x) < total) tile_coords<BN, SWAP>(p, blockIdx.x, pre_pi, pre_m0, pre_n0);
     // Everything above reads no argument buffer; from here on every role
     // reads inputs (or writes outputs that an earlier kernel may still read).
     grid_dependency_wait();
@@ -853,12 +857,19 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
             int tl = s / KB, kbn = s % KB, cur_tl = -1;
             int pi = 0, m0 = 0, n0 = 0;
             for (uint32_t g = s; g < ng; g += STAGES) {
-                if (!wait_bounded(smem_u32(&empty[s]), ((g / STAGES) & 1) ^ 1, abort_flag, tmo)) {
+                // (The ring's first pass needs no wait: every stage starts free.)
+                if (g >= STAGES && !wait_bounded(smem_u32(&empty[s]), ((g / STAGES) & 1) ^ 1, abort_flag, tmo)) {
                     ok = false;
                     break;
                 }
                 if (tl != cur_tl) {
-                    tile_coords<BN, SWAP>(p, blockIdx.x + tl * gridDim.x, pi, m0, n0);
+                    if (tl == 0) {
+                        pi = pre_pi;
+                        m0 = pre_m0;
+                        n0 = pre_n0;
+                    } else {
+                        tile_coords<BN, SWAP>(p, blockIdx.x + tl * gridDim.x, pi, m0, n0);
+                    }
                     cur_tl = tl;
                 }
                 const int kb = kbn;
