@@ -50,6 +50,9 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 KQ, KKV, N_ATTN, N_IDX = 1536, 512, 24576, 4096
+# Back-to-back decode calls per CUDA graph (the steady state of a decode loop,
+# which runs every layer's kernels one after another).
+DECODE_GRAPH_CALLS = 32
 METRIC = "norm+quant HBM GB/s (% of peak) & µs at M=1; block-scaled FP8 GEMM TFLOPS"
 NQ_BYTES_PER_ROW = 2 * KQ + 2 * KKV + KQ + 4 * (KQ // 128) + 2 * KKV   # 6704
 NQ_BYTES_PER_CALL = 2 * (KQ + KKV)                                      # gammas
@@ -452,8 +455,9 @@ def decode_sweep(torch, dsnq, inputs, dev, flush, hbm_gbs):
 
 def decode_step(torch, dsnq, inputs, dev, flush, buf, gq, gkv, eps, qo, so, ko):
     """One decode step at M=1 (fused norm+quant, then the dual GEMM on its
-    output): a CUDA graph of 8 steps on 8 cold rows, cycling over 4 copies of
-    the weights (176 MB, more than L2), with launch overlap on and off."""
+    output): a CUDA graph of DECODE_GRAPH_CALLS steps on as many cold rows,
+    cycling over 4 copies of the weights (176 MB, more than L2), with launch
+    overlap on and off."""
     stream = torch.cuda.current_stream()
     wa, swa = dsnq.quantize_weight_block128(inputs.weight(N_ATTN, KQ, seed=0, salt=1).to(dev))
     wi, swi = dsnq.quantize_weight_block128(inputs.weight(N_IDX, KQ, seed=0, salt=2).to(dev))
@@ -466,7 +470,8 @@ def decode_step(torch, dsnq, inputs, dev, flush, buf, gq, gkv, eps, qo, so, ko):
                                             q_out=qo, q_scale=so, kv_out=ko)
         dsnq.block_scaled_fp8_gemm_dual(qo, so, c[0], c[1], c[2], c[3], out1=oa, out2=oi)
 
-    steps = [(lambda r=r: step(r, copies[r % 4])) for r in range(8)]
+    n_steps = DECODE_GRAPH_CALLS
+    steps = [(lambda r=r: step(r, copies[r % 4])) for r in range(n_steps)]
     res = {}
     for overlap in (True, False):
         dsnq.set_launch_overlap(overlap)
@@ -475,10 +480,10 @@ def decode_step(torch, dsnq, inputs, dev, flush, buf, gq, gkv, eps, qo, so, ko):
 
     # bf16 activations without a pre-quantized pair: quantized inside the GEMM
     # (one launch) against the quant kernel followed by the GEMM.
-    xa = inputs.activations_bf16(8, KQ, seed=9).to(dev)
+    xa = inputs.activations_bf16(n_steps, KQ, seed=9).to(dev)
     so_col = dsnq.empty_scales(1, KQ // 128, "col", dev)
     in_gemm = [(lambda r=r: dsnq.block_scaled_fp8_gemm_dual_bf16a(xa[r:r + 1], *copies[r % 4], out1=oa, out2=oi))
-               for r in range(8)]
+               for r in range(n_steps)]
 
     def two_launches(r):
         dsnq.group_quant_bf16(xa[r:r + 1], scale_layout="col", x_out=qo, x_scale=so_col)
@@ -486,13 +491,13 @@ def decode_step(torch, dsnq, inputs, dev, flush, buf, gq, gkv, eps, qo, so, ko):
 
     res["bf16_in_gemm_quant"] = round(timed_graph_calls(torch, stream, in_gemm, flush), 3)
     res["bf16_quant_then_gemm"] = round(timed_graph_calls(torch, stream, [(lambda r=r: two_launches(r))
-                                                                          for r in range(8)], flush), 3)
+                                                                          for r in range(n_steps)], flush), 3)
     one = [(lambda r=r: dsnq.fused_norm_quant_gemm_dual(buf[r:r + 1, :KQ], buf[r:r + 1, KQ:KQ + KKV], gq, gkv, eps,
                                                         *copies[r % 4], out1=oa, out2=oi, kv_out=ko))
-           for r in range(8)]
+           for r in range(n_steps)]
     res["one_launch"] = round(timed_graph_calls(torch, stream, one, flush), 3)
-    res["note"] = ("us per step: fused norm+quant then the dual GEMM (44 MB of weights from HBM), CUDA graph of 8 "
-                   "steps on 8 cold rows over 4 weight copies; overlap = programmatic dependent launch (default); "
+    res["note"] = ("us per step: fused norm+quant then the dual GEMM (44 MB of weights from HBM), CUDA graph of "
+                   f"{n_steps} steps on {n_steps} cold rows over 4 weight copies; overlap = programmatic dependent launch (default); "
                    "one_launch: the same step with the norm+quant inside the GEMM; "
                    "bf16_*: the dual GEMM on a bf16 row quantized inside the GEMM, or by the quant kernel first")
     return res
@@ -519,14 +524,15 @@ def gemm_sweep(torch, dsnq, inputs, dev, flush, hbm_gbs, args, fp8_peak):
                        "gbs": round(byt / (us * 1e-6) / 1e9, 1),
                        "frac_hbm": round(byt / (us * 1e-6) / 1e9 / hbm_gbs, 4)}
         if M <= 128:
-            # Back-to-back calls as in a decode loop: a CUDA graph of 8 calls over
-            # 4 copies of the weights (176 MB, more than L2), so each call streams
-            # its weights from HBM without the per-launch host and event overhead.
+            # Back-to-back calls as in a decode loop: a CUDA graph of
+            # DECODE_GRAPH_CALLS calls over 4 copies of the weights (176 MB, more
+            # than L2), so each call streams its weights from HBM without the
+            # per-launch host and event overhead.
             if not copies:
                 copies.extend([(wa, swa, wi, swi)] + [(wa.clone(), swa.clone(), wi.clone(), swi.clone())
                                                       for _ in range(3)])
             calls = [(lambda c=copies[i % 4]: dsnq.block_scaled_fp8_gemm_dual(
-                a, sa, c[0], c[1], c[2], c[3], out1=oa, out2=oi)) for i in range(8)]
+                a, sa, c[0], c[1], c[2], c[3], out1=oa, out2=oi)) for i in range(DECODE_GRAPH_CALLS)]
             gus = timed_graph_calls(torch, stream, calls, flush, reps=max(args.side_reps, 5))
             res[str(M)].update({"graph_us": round(gus, 3), "graph_gbs": round(byt / (gus * 1e-6) / 1e9, 1),
                                 "graph_frac_hbm": round(byt / (gus * 1e-6) / 1e9 / hbm_gbs, 4)})
@@ -547,7 +553,7 @@ def gemm_sweep(torch, dsnq, inputs, dev, flush, hbm_gbs, args, fp8_peak):
                                           "kernel": "pair_gemm_kernel", "N": N_ATTN}
         del q8, s8, oa
     res["note"] = ("column-major activation scales; us: one launch timed with CUDA events after an L2 flush (includes "
-                   "launch latency); graph_us: per call in a CUDA graph of 8 back-to-back calls over 4 weight copies "
+                   f"launch latency); graph_us: per call in a CUDA graph of {DECODE_GRAPH_CALLS} back-to-back calls over 4 weight copies "
                    "(cold in L2); 32768_long_context_attn: the long-context stress rows quantized by the fused kernel, "
                    "then the attention wq_b GEMM alone (N=24576)")
     return res
