@@ -68,6 +68,33 @@ def test_matches_oracle(M):
     assert torch.equal(o1, t1) and torch.equal(o2, t2)
 
 
+@pytest.mark.parametrize("M,Kq", [(1, 1408), (3, 1408), (6, 1408), (1, 2048), (2, 2048), (5, 512)])
+def test_one_launch_other_widths(M, Kq):
+    """The one-launch route at other q widths: an odd number of K blocks (the
+    last 256-column unit half past the row), the widest row it takes (eight
+    units), and a narrow one; one to six rows spread over the quantizer warps."""
+    assert dsnq.fused_quant_fits(M, Kq)
+    g = torch.Generator().manual_seed(90 + M + Kq)
+    q = (torch.randn(M, Kq, generator=g) * 2.0).to(torch.bfloat16)
+    kv = torch.randn(M, 512, generator=g).to(torch.bfloat16)
+    gq, gkv = inputs.gammas(91, Kq, 512)
+    w1, s1 = quantized_weight(384, Kq, seed=92)
+    w2, s2 = quantized_weight(256, Kq, seed=93)
+    W = dev(w1, s1, w2, s2)
+    o1, o2, kvo, qf, qs = run(q.cuda(), kv.cuda(), gq.cuda(), gkv.cuda(), 1e-6, W)
+    torch.cuda.synchronize()
+    codes, scale, kv_bits = oracle.fused_dual_rmsnorm_group_quant(
+        inputs.bits(q), inputs.bits(kv), inputs.bits(gq), inputs.bits(gkv), 1e-6)
+    assert_codes_close(qf.view(torch.uint8).cpu().numpy(), codes)
+    assert_scales_close(qs.cpu().numpy(), scale)
+    assert_bf16_close(kvo.view(torch.int16).cpu().numpy().view(np.uint16), kv_bits)
+    for out, wc, ws in ((o1, w1, s1), (o2, w2, s2)):
+        ref = oracle.block_scaled_gemm(codes, scale, wc, ws)
+        assert rel_fro(bf16_value(out), ref) <= GEMM_REL_FRO
+    t1, t2 = dsnq.block_scaled_fp8_gemm_dual(qf, qs, *W)
+    assert torch.equal(o1, t1) and torch.equal(o2, t2)
+
+
 def test_one_launch_without_q_outputs():
     lat = inputs.decode_batch(3, seed=80)
     q, kv = on_device(lat)
