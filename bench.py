@@ -825,7 +825,8 @@ def allreduce_max(x: float, world, dev):
 def run_kernel_only(args):
     """A few launches of one kernel on the configured workload, for profilers
     (ncu): `--kernel-only gemm` runs the dual GEMM, `norm_quant` the fused
-    norm+quant; no timing, no JSON line."""
+    norm+quant, `fused_step` the one-launch norm+quant+GEMM (a few decode
+    rows); no timing, no JSON line."""
     import torch
     import gemm_dsnq_dual_gb300 as dsnq
     from gemm_dsnq_dual_gb300 import inputs
@@ -835,10 +836,14 @@ def run_kernel_only(args):
     q, kv = lat.q.to(dev), lat.kv.to(dev)
     gq, gkv = lat.gamma_q.to(dev), lat.gamma_kv.to(dev)
     q8, s8, _ = dsnq.fused_dual_rmsnorm_group_quant(q, kv, gq, gkv, lat.eps, scale_layout="col")
-    if args.kernel_only == "gemm":
+    if args.kernel_only in ("gemm", "fused_step"):
         wa, swa = dsnq.quantize_weight_block128(inputs.weight(N_ATTN, KQ, seed=0, salt=1).to(dev))
         wi, swi = dsnq.quantize_weight_block128(inputs.weight(N_IDX, KQ, seed=0, salt=2).to(dev))
+    if args.kernel_only == "gemm":
         fn = lambda: dsnq.block_scaled_fp8_gemm_dual(q8, s8, wa, swa, wi, swi)
+    elif args.kernel_only == "fused_step":
+        # The decode step as one launch (norm+quant inside the GEMM's prologue).
+        fn = lambda: dsnq.fused_norm_quant_gemm_dual(q, kv, gq, gkv, lat.eps, wa, swa, wi, swi)
     else:
         fn = lambda: dsnq.fused_dual_rmsnorm_group_quant(q, kv, gq, gkv, lat.eps, scale_layout="col",
                                                          q_out=q8, q_scale=s8)
@@ -862,7 +867,7 @@ def main():
     ap.add_argument("--no-long-context", dest="long_context", action="store_false",
                     help="skip the M=32768 long-context GEMM of the side measurements")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--kernel-only", choices=["gemm", "norm_quant"], default=None,
+    ap.add_argument("--kernel-only", choices=["gemm", "norm_quant", "fused_step"], default=None,
                     help="profiling aid: launch one kernel --launches times and exit")
     ap.add_argument("--launches", type=int, default=3)
     ap.add_argument("--oracle-child", type=int, default=0, help=argparse.SUPPRESS)
