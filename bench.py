@@ -317,6 +317,11 @@ def headline(line: dict) -> dict:
     if "32768_long_context_attn" in gs:
         h["gemm_attn_M32768_tflops"] = gs["32768_long_context_attn"]["tflops"]
         h["gemm_attn_M32768_frac_fp8"] = gs["32768_long_context_attn"]["frac_fp8"]
+    sl = line.get("single_latent_norm_quant", {})
+    if "1" in sl:
+        h["single_latent_us_at_M1"] = sl["1"]["graph_us"]
+        h["single_latent_graph_frac_hbm"] = {m: v["graph_frac_hbm"] for m, v in sl.items()
+                                             if isinstance(v, dict) and m != "1"}
     ds = line.get("decode_sweep", {})
     h["norm_quant_decode_us"] = {m: [v["row_us"], v["col_us"]] for m, v in ds.items() if isinstance(v, dict)}
     cb = line.get("cpu_baseline")
@@ -421,11 +426,43 @@ def side_measurements(torch, dsnq, inputs, dev, flush, hbm_gbs, args, fp8_peak):
             del sets, calls
         del q, kv, qf, sc, ko2, qb, qf2, sc2
     out["norm_quant_sweep"] = sweep
+    out["single_latent_norm_quant"] = single_latent(torch, dsnq, inputs, dev, flush, hbm_gbs, args)
     out["norm_quant_sweep_note"] = ("fused_us / unfused: single launches timed with CUDA events, L2 flushed before "
                                     "each (includes launch latency); fused_graph_us: per call in a CUDA graph of "
                                     "back-to-back calls over graph_sets distinct input/output sets (> 160 MiB in "
                                     "total, more than L2); M=8192 uses the prefill Student-t inputs, column-major scales")
     return out
+
+
+def single_latent(torch, dsnq, inputs, dev, flush, hbm_gbs, args):
+    """The single-latent RMSNorm + per-1x128 quant (the q latent alone,
+    [M, 1536] bf16 -> codes + column-major scales): per call in CUDA graphs,
+    M=1 over 100 cold rows and the larger M over input/output sets that
+    exceed L2.  Bytes per row: 3072 read, 1536 + 48 written."""
+    stream = torch.cuda.current_stream()
+    per_row, per_call = KQ * 2 + KQ + 4 * (KQ // 128), KQ * 2
+    res = {}
+    for M in [1] + [m for m in args.nq_sweep if m >= 1024]:
+        x = inputs.full_path_batch(max(M, 100), seed=7).q.to(dev)
+        gq = inputs.gammas(8)[0].to(dev)
+        if M == 1:
+            qf = torch.empty(1, KQ, dtype=torch.float8_e4m3fn, device=dev)
+            sc = dsnq.empty_scales(1, KQ // 128, "col", dev)
+            calls = [(lambda r=r: dsnq.rmsnorm_group_quant(x[r:r + 1], gq, 1e-6, scale_layout="col",
+                                                           x_out=qf, x_scale=sc)) for r in range(100)]
+        else:
+            nsets = max(2, -(-160 * 2 ** 20 // (M * per_row)))
+            sets = [(x[:M].clone(), torch.empty(M, KQ, dtype=torch.float8_e4m3fn, device=dev),
+                     dsnq.empty_scales(M, KQ // 128, "col", dev)) for _ in range(nsets)]
+            calls = [(lambda s=s: dsnq.rmsnorm_group_quant(s[0], gq, 1e-6, scale_layout="col", x_out=s[1],
+                                                           x_scale=s[2])) for s in sets]
+        us = timed_graph_calls(torch, stream, calls, flush, reps=max(args.side_reps, 5))
+        gbs = (M * per_row + per_call) / (us * 1e-6) / 1e9
+        res[str(M)] = {"graph_us": round(us, 3), "graph_gbs": round(gbs, 1), "graph_frac_hbm": round(gbs / hbm_gbs, 4)}
+        del calls, x
+    res["note"] = ("per call in a CUDA graph: M=1 over 100 distinct cold rows, larger M over distinct input/output "
+                   "sets of more than 160 MiB in total; L2 flushed per replay")
+    return res
 
 
 def decode_sweep(torch, dsnq, inputs, dev, flush, hbm_gbs):

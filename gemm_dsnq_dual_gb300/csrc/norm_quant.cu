@@ -436,7 +436,8 @@ __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_gr
 template <int QS, int KS>
 __global__ void __launch_bounds__(kFusedWarps * 32, kFusedCtasPerSM)
 warp_row_fused_kernel(const RowArgs a) {
-    static_assert(QS == 6 && KS == 2, "the lane roles below are laid out for the DSv4 row");
+    // KS = 0: the single-latent call (the q latent alone; no kv chunk is touched).
+    static_assert(QS == 6 && (KS == 2 || KS == 0), "the lane roles below are laid out for the DSv4 row");
     grid_dependency_wait();      // inputs are read only once the previous kernel's writes are visible
     allow_dependent_launch();
     bounds_self_test(a.inject);
@@ -446,7 +447,7 @@ warp_row_fused_kernel(const RowArgs a) {
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     constexpr int kq = QS * 256, width = CPT * 256;
-    static_assert(CPT * 256 * 2 == kDsv4RowBytes, "ring slots hold one row");
+    static_assert(CPT * 256 * 2 <= kDsv4RowBytes, "ring slots hold one row");
     const bool q_half = lane < 16;              // reduce-scatter roles
     const bool hi8 = (lane & 8) != 0;
     const int gi = lane & 7;                    // group slot this lane forms (when < 3)
@@ -606,6 +607,7 @@ warp_row_fused_kernel(const RowArgs a) {
 
 // The staged kernel's shared memory is above the default 48 KB limit; the
 // attribute is set once per device.
+template <int KS>
 static bool fused_smem_ready() {
     static std::mutex mu;
     static bool done[64] = {};
@@ -613,7 +615,7 @@ static bool fused_smem_ready() {
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
     std::lock_guard<std::mutex> lock(mu);
     if (!done[dev]) {
-        if (cudaFuncSetAttribute(warp_row_fused_kernel<6, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(warp_row_fused_kernel<6, KS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(fused_smem_bytes())) != cudaSuccess)
             return false;
         done[dev] = true;
@@ -631,13 +633,16 @@ static dsnq_status launch_rows(RowArgs a, int64_t M, cudaStream_t s) {
     // Many rows: one warp per row (no block barrier per row).  Few rows: a
     // warp-group per row, which shortens each thread's dependency chain.
     const int64_t warp_row_min = sms > 0 ? static_cast<int64_t>(sms) * 8 : 2048;
-    if (MODE == kFused && a.cq == 6 * 32 && a.ckv == 2 * 32 && M >= warp_row_min) {
-        // DSv4 rows (Kq = 1536, Kkv = 512): the specialized warp-per-row kernel.
-        if (!fused_smem_ready()) return DSNQ_ERR_CUDA;
+    if (MODE == kFused && a.cq == 6 * 32 && (a.ckv == 2 * 32 || a.ckv == 0) && M >= warp_row_min) {
+        // DSv4 rows (Kq = 1536, Kkv = 512, or the q latent alone): the
+        // specialized warp-per-row kernel.
+        const bool with_kv = a.ckv != 0;
+        if (!(with_kv ? fused_smem_ready<2>() : fused_smem_ready<0>())) return DSNQ_ERR_CUDA;
         const int64_t rows_cap = sms > 0 ? static_cast<int64_t>(sms) * kFusedCtasPerSM : (M + kFusedWarps - 1) / kFusedWarps;
         const int64_t need = (M + kFusedWarps - 1) / kFusedWarps;
         dim3 grid(static_cast<unsigned>(need < rows_cap ? need : rows_cap)), block(kFusedWarps * 32);
-        return launch_result(launch_kernel(warp_row_fused_kernel<6, 2>, grid, block, fused_smem_bytes(), s, a));
+        return launch_result(with_kv ? launch_kernel(warp_row_fused_kernel<6, 2>, grid, block, fused_smem_bytes(), s, a)
+                                     : launch_kernel(warp_row_fused_kernel<6, 0>, grid, block, fused_smem_bytes(), s, a));
     }
     if (chunks <= 8 * 32 && M >= warp_row_min) {
         // Warp per row.  Enough CTAs to fill every SM at the register-limited occupancy.

@@ -73,6 +73,7 @@ def test_headline_keeps_the_metric_numbers():
             "gemm_sweep": {"1": {"graph_us": 10.8, "graph_frac_hbm": 0.6}, "1024": {"tflops": 1600.0},
                            "32768_long_context_attn": {"tflops": 2000.0, "frac_fp8": 0.52}},
             "decode_sweep": {"1": {"row_us": 2.5, "col_us": 2.5}, "note": "x"},
+            "single_latent_norm_quant": {"1": {"graph_us": 2.2}, "8192": {"graph_frac_hbm": 0.6}, "note": "x"},
             "cpu_baseline": {"cores": 16, "value": 0.1, "single_thread": {"value": 0.02}}}
     h = bench.headline(line)
     assert h["norm_quant_us_at_M1"] == 2.4
@@ -80,6 +81,7 @@ def test_headline_keeps_the_metric_numbers():
     assert h["gemm_attn_M32768_frac_fp8"] == 0.52 and h["gemm_dual_M8192_frac_fp8"] == 0.51
     assert h["norm_quant_decode_us"] == {"1": [2.5, 2.5]}
     assert h["decode_step_us_at_M1"] == 13.0 and h["decode_step_us_at_M1_one_launch"] == 12.3
+    assert h["single_latent_us_at_M1"] == 2.2 and h["single_latent_graph_frac_hbm"] == {"8192": 0.6}
     assert h["cpu_oracle_tflops"] == {"cores": 16, "all": 0.1, "one_thread": 0.02}
 
 

@@ -270,8 +270,11 @@ def test_single_latent_rmsnorm_group_quant(M, K, layout):
     assert_codes_close(u8(codes), wc)
 
 
-def test_single_latent_zero_rows_and_matches_fused_q_part():
-    lat = inputs.decode_batch(16, seed=12)
+@pytest.mark.parametrize("M", [16, 4096])
+def test_single_latent_zero_rows_and_matches_fused_q_part(M):
+    """The q latent alone gives the q part of the dual call bit for bit, with
+    few rows (warp-group kernel) and many (warp-per-row kernel)."""
+    lat = inputs.decode_batch(M, seed=12)
     q, kv = to_device(lat)
     gq, gkv = lat.gamma_q.cuda(), lat.gamma_kv.cuda()
     c1, s1 = dsnq.rmsnorm_group_quant(q, gq, lat.eps)
