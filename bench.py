@@ -53,6 +53,10 @@ KQ, KKV, N_ATTN, N_IDX = 1536, 512, 24576, 4096
 # Back-to-back decode calls per CUDA graph (the steady state of a decode loop,
 # which runs every layer's kernels one after another).
 DECODE_GRAPH_CALLS = 32
+# Norm+quant at M >= 1024: calls per CUDA graph (at least), cycling over
+# distinct input/output sets; a set is revisited only after more than L2's
+# worth of other sets (cold every time).
+NQ_GRAPH_CALLS = 16
 METRIC = "norm+quant HBM GB/s (% of peak) & µs at M=1; block-scaled FP8 GEMM TFLOPS"
 NQ_BYTES_PER_ROW = 2 * KQ + 2 * KKV + KQ + 4 * (KQ // 128) + 2 * KKV   # 6704
 NQ_BYTES_PER_CALL = 2 * (KQ + KKV)                                      # gammas
@@ -330,6 +334,13 @@ def headline(line: dict) -> dict:
     return h
 
 
+def graph_sets(bytes_per_set):
+    """Distinct input/output sets for a graph that cycles over them: enough
+    that more than 160 MiB (more than L2) of other sets pass between two
+    visits of one set."""
+    return 1 + max(1, -(-160 * 2 ** 20 // bytes_per_set))
+
+
 def timed_graph_calls(torch, stream, fn_list, flush, reps=20):
     """Replays a CUDA graph of len(fn_list) calls `reps` times, L2 flushed
     before each replay; returns the median per-call time in microseconds."""
@@ -410,27 +421,29 @@ def side_measurements(torch, dsnq, inputs, dev, flush, hbm_gbs, args, fp8_peak):
                          "fused_frac_hbm": round(gbs / hbm_gbs, 4),
                          "unfused_3_kernels_us": round(u_us, 3),
                          "speedup_vs_unfused": round(u_us / f_us, 3)}
-        # Back-to-back calls: a CUDA graph over distinct input/output sets
-        # whose total exceeds L2, so every call reads from and writes to HBM.
-        nsets = max(2, -(-160 * 2 ** 20 // (M * NQ_BYTES_PER_ROW)))
+        # Back-to-back calls: a CUDA graph cycling over distinct input/output
+        # sets, so every call reads from and writes to HBM.
+        nsets = graph_sets(M * NQ_BYTES_PER_ROW)
         if nsets * M * NQ_BYTES_PER_ROW <= 2 * 2 ** 30:
             sets = [(q.clone(), kv.clone(), torch.empty_like(qf), dsnq.empty_scales(M, KQ // 128, "col", dev),
                      torch.empty_like(ko2)) for _ in range(nsets)]
-            calls = [(lambda t=t: dsnq.fused_dual_rmsnorm_group_quant(
+            calls = [(lambda t=sets[i % nsets]: dsnq.fused_dual_rmsnorm_group_quant(
                 t[0], t[1], gq2, gkv2, lat.eps, scale_layout="col", q_out=t[2], q_scale=t[3], kv_out=t[4]))
-                for t in sets]
+                for i in range(max(nsets, NQ_GRAPH_CALLS))]
             g_us = timed_graph_calls(torch, stream, calls, flush, reps=max(args.side_reps, 5))
             g_gbs = (M * NQ_BYTES_PER_ROW + NQ_BYTES_PER_CALL) / (g_us * 1e-6) / 1e9
             sweep[str(M)].update({"fused_graph_us": round(g_us, 3), "fused_graph_gbs": round(g_gbs, 1),
-                                  "fused_graph_frac_hbm": round(g_gbs / hbm_gbs, 4), "graph_sets": nsets})
+                                  "fused_graph_frac_hbm": round(g_gbs / hbm_gbs, 4), "graph_sets": nsets,
+                                  "graph_calls": len(calls)})
             del sets, calls
         del q, kv, qf, sc, ko2, qb, qf2, sc2
     out["norm_quant_sweep"] = sweep
     out["single_latent_norm_quant"] = single_latent(torch, dsnq, inputs, dev, flush, hbm_gbs, args)
     out["norm_quant_sweep_note"] = ("fused_us / unfused: single launches timed with CUDA events, L2 flushed before "
                                     "each (includes launch latency); fused_graph_us: per call in a CUDA graph of "
-                                    "back-to-back calls over graph_sets distinct input/output sets (> 160 MiB in "
-                                    "total, more than L2); M=8192 uses the prefill Student-t inputs, column-major scales")
+                                    "graph_calls back-to-back calls cycling over graph_sets distinct input/output sets "
+                                    "(a set comes back only after more than 160 MiB of others, more than L2); M=8192 "
+                                    "uses the prefill Student-t inputs, column-major scales")
     return out
 
 
@@ -451,17 +464,19 @@ def single_latent(torch, dsnq, inputs, dev, flush, hbm_gbs, args):
             calls = [(lambda r=r: dsnq.rmsnorm_group_quant(x[r:r + 1], gq, 1e-6, scale_layout="col",
                                                            x_out=qf, x_scale=sc)) for r in range(100)]
         else:
-            nsets = max(2, -(-160 * 2 ** 20 // (M * per_row)))
+            nsets = graph_sets(M * per_row)
             sets = [(x[:M].clone(), torch.empty(M, KQ, dtype=torch.float8_e4m3fn, device=dev),
                      dsnq.empty_scales(M, KQ // 128, "col", dev)) for _ in range(nsets)]
-            calls = [(lambda s=s: dsnq.rmsnorm_group_quant(s[0], gq, 1e-6, scale_layout="col", x_out=s[1],
-                                                           x_scale=s[2])) for s in sets]
+            calls = [(lambda s=sets[i % nsets]: dsnq.rmsnorm_group_quant(s[0], gq, 1e-6, scale_layout="col",
+                                                                         x_out=s[1], x_scale=s[2]))
+                     for i in range(max(nsets, NQ_GRAPH_CALLS))]
         us = timed_graph_calls(torch, stream, calls, flush, reps=max(args.side_reps, 5))
         gbs = (M * per_row + per_call) / (us * 1e-6) / 1e9
         res[str(M)] = {"graph_us": round(us, 3), "graph_gbs": round(gbs, 1), "graph_frac_hbm": round(gbs / hbm_gbs, 4)}
         del calls, x
-    res["note"] = ("per call in a CUDA graph: M=1 over 100 distinct cold rows, larger M over distinct input/output "
-                   "sets of more than 160 MiB in total; L2 flushed per replay")
+    res["note"] = ("per call in a CUDA graph: M=1 over 100 distinct cold rows, larger M as at least "
+                   f"{NQ_GRAPH_CALLS} calls cycling over distinct input/output sets (a set comes back only after more "
+                   "than 160 MiB of others); L2 flushed per replay")
     return res
 
 

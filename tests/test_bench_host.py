@@ -10,6 +10,16 @@ import pytest
 import bench
 
 
+@pytest.mark.parametrize("M", [1024, 2048, 8192, 32768])
+def test_graph_sets_keep_every_call_cold(M):
+    """A graph cycling over the sets revisits one only after more than L2's
+    worth (160 MiB) of the others."""
+    per_set = M * bench.NQ_BYTES_PER_ROW
+    n = bench.graph_sets(per_set)
+    assert n >= 2 and (n - 1) * per_set > 160 * 2 ** 20
+    assert (n - 2) * per_set <= 160 * 2 ** 20 or n == 2      # no more sets than that needs
+
+
 def test_algorithmic_units():
     # Fused norm+quant per row: q 3072 + kv 1024 read; codes 1536 + 12 fp32
     # scales + kv 1024 written.  Unfused: norm (4096 in, 4096 out) and two
