@@ -877,8 +877,11 @@ def allreduce_max(x: float, world, dev):
 def run_kernel_only(args):
     """A few launches of one kernel on the configured workload, for profilers
     (ncu): `--kernel-only gemm` runs the dual GEMM, `norm_quant` the fused
-    norm+quant, `fused_step` the one-launch norm+quant+GEMM (a few decode
-    rows); no timing, no JSON line."""
+    norm+quant, `single_latent` the single-latent norm+quant of q,
+    `unfused` the unfused baseline's three launches (norm to bf16, then the
+    quant of q twice), `fused_step` the one-launch norm+quant+GEMM (a few
+    decode rows); no timing, no JSON line.  Every mode first runs one fused
+    norm+quant to make its inputs."""
     import torch
     import gemm_dsnq_dual_gb300 as dsnq
     from gemm_dsnq_dual_gb300 import inputs
@@ -896,6 +899,17 @@ def run_kernel_only(args):
     elif args.kernel_only == "fused_step":
         # The decode step as one launch (norm+quant inside the GEMM's prologue).
         fn = lambda: dsnq.fused_norm_quant_gemm_dual(q, kv, gq, gkv, lat.eps, wa, swa, wi, swi)
+    elif args.kernel_only == "single_latent":
+        fn = lambda: dsnq.rmsnorm_group_quant(q, gq, lat.eps, scale_layout="col", x_out=q8, x_scale=s8)
+    elif args.kernel_only == "unfused":
+        qb = torch.empty(M, KQ, dtype=torch.bfloat16, device=dev)
+        kb = torch.empty(M, KKV, dtype=torch.bfloat16, device=dev)
+        q8b, s8b = torch.empty_like(q8), dsnq.empty_scales(M, KQ // 128, "col", dev)
+
+        def fn():
+            dsnq.dual_rmsnorm_bf16(q, kv, gq, gkv, lat.eps, q_out=qb, kv_out=kb)
+            dsnq.group_quant_bf16(qb, scale_layout="col", x_out=q8, x_scale=s8)
+            dsnq.group_quant_bf16(qb, scale_layout="col", x_out=q8b, x_scale=s8b)
     else:
         fn = lambda: dsnq.fused_dual_rmsnorm_group_quant(q, kv, gq, gkv, lat.eps, scale_layout="col",
                                                          q_out=q8, q_scale=s8)
@@ -919,7 +933,8 @@ def main():
     ap.add_argument("--no-long-context", dest="long_context", action="store_false",
                     help="skip the M=32768 long-context GEMM of the side measurements")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--kernel-only", choices=["gemm", "norm_quant", "fused_step"], default=None,
+    ap.add_argument("--kernel-only", choices=["gemm", "norm_quant", "single_latent", "unfused", "fused_step"],
+                    default=None,
                     help="profiling aid: launch one kernel --launches times and exit")
     ap.add_argument("--launches", type=int, default=3)
     ap.add_argument("--oracle-child", type=int, default=0, help=argparse.SUPPRESS)
