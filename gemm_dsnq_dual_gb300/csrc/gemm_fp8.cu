@@ -593,8 +593,8 @@ __device__ __forceinline__ void norm_quantize_activations(const Params& p, uint8
     const int K = KB * kBK;
     if (!bounds_ok(units <= kU * nw && slots <= kMaxSlots && live <= 16)) return;   // (debug build) outside the dispatch bound
 
-    int row[kU], slot[kU];
-    bool on[kU], in[kU];
+    int row[kU] = {}, slot[kU] = {};
+    bool on[kU] = {}, in[kU] = {};
     // The lane's chunk of unit j (odd KB: the last slot's second half is past
     // the row and reads as zero).
     auto load_unit = [&](int j) {
