@@ -52,11 +52,11 @@ if ROOT not in sys.path:
 KQ, KKV, N_ATTN, N_IDX = 1536, 512, 24576, 4096
 # Back-to-back decode calls per CUDA graph (the steady state of a decode loop,
 # which runs every layer's kernels one after another).
-DECODE_GRAPH_CALLS = 32
+DECODE_GRAPH_CALLS = 100
 # Norm+quant at M >= 1024: calls per CUDA graph (at least), cycling over
 # distinct input/output sets; a set is revisited only after more than L2's
 # worth of other sets (cold every time).
-NQ_GRAPH_CALLS = 16
+NQ_GRAPH_CALLS = 100
 METRIC = "norm+quant HBM GB/s (% of peak) & µs at M=1; block-scaled FP8 GEMM TFLOPS"
 NQ_BYTES_PER_ROW = 2 * KQ + 2 * KKV + KQ + 4 * (KQ // 128) + 2 * KKV   # 6704
 NQ_BYTES_PER_CALL = 2 * (KQ + KKV)                                      # gammas
@@ -372,7 +372,7 @@ def side_measurements(torch, dsnq, inputs, dev, flush, hbm_gbs, args, fp8_peak):
     stream = torch.cuda.current_stream()
     out = {}
     # -- M=1 decode latency: 100 calls, each on its own cold row of a split-view buffer
-    n = 100
+    n = max(100, DECODE_GRAPH_CALLS)       # the decode step below takes its cold rows from here too
     dec = inputs.decode_batch(n, seed=1)
     buf = dec.buf.to(dev)
     gq, gkv = dec.gamma_q.to(dev), dec.gamma_kv.to(dev)
@@ -483,11 +483,12 @@ def single_latent(torch, dsnq, inputs, dev, flush, hbm_gbs, args):
 def decode_sweep(torch, dsnq, inputs, dev, flush, hbm_gbs):
     """Norm+quant at the decode batch sizes, on strided split views of one
     [M, 2112] buffer per call, in both scale layouts: us per call in a CUDA
-    graph of 32 calls on 32 distinct cold batches (L2 flushed per replay)."""
+    graph of DECODE_GRAPH_CALLS calls on as many distinct cold batches (L2
+    flushed per replay)."""
     stream = torch.cuda.current_stream()
     res = {}
     for M in (1, 2, 8, 32, 64):
-        dec = inputs.decode_batch(32 * M, seed=1)
+        dec = inputs.decode_batch(DECODE_GRAPH_CALLS * M, seed=1)
         buf = dec.buf.to(dev)
         gq, gkv = dec.gamma_q.to(dev), dec.gamma_kv.to(dev)
         qo = torch.empty(M, KQ, dtype=torch.float8_e4m3fn, device=dev)
@@ -497,10 +498,11 @@ def decode_sweep(torch, dsnq, inputs, dev, flush, hbm_gbs):
             so = dsnq.empty_scales(M, KQ // 128, lay, dev)
             calls = [(lambda i=i: dsnq.fused_dual_rmsnorm_group_quant(
                 buf[i * M:(i + 1) * M, :KQ], buf[i * M:(i + 1) * M, KQ:KQ + KKV], gq, gkv, dec.eps, scale_layout=lay,
-                q_out=qo, q_scale=so, kv_out=ko)) for i in range(32)]
+                q_out=qo, q_scale=so, kv_out=ko)) for i in range(DECODE_GRAPH_CALLS)]
             r[lay + "_us"] = round(timed_graph_calls(torch, stream, calls, flush), 3)
         res[str(M)] = r
-    res["note"] = ("us per call: CUDA graph of 32 calls on 32 distinct cold batches of split views (row stride 2112), "
+    res["note"] = (f"us per call: CUDA graph of {DECODE_GRAPH_CALLS} calls on as many distinct cold batches of split "
+                   "views (row stride 2112), "
                    "L2 flushed per replay; row = [M,12] scales, col = [12,M] (transpose_scale)")
     return res
 
