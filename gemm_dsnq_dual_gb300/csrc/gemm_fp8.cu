@@ -451,8 +451,14 @@ struct Cfg {
     static constexpr int kPBytes = kPRows * kBK;       // 16 KB
     static constexpr int kQBytes = AQ ? 0 : BN * kBK;
     static constexpr int kStageBytes = kPBytes + kQBytes;
-    static constexpr int kResBytes = BN * kBK;         // AQ: one K block of the resident operand
+    // AQ: one K block of the resident operand holds kResRows rows (the few
+    // live ones, then zeros).  The MMA reads BN rows from each K block's
+    // base, so rows kResRows.. are the next K block's first rows (one spare
+    // block after the last): garbage in token columns no call stores.
+    static constexpr int kResRows = 8;
+    static constexpr int kResBytes = kResRows * kBK;
     static_assert(!AQ || SWAP, "in-kernel activation quant is a decode (swap-AB) variant");
+    static_assert(!AQ || (BN == 16 && kResRows * kBK == 1024), "resident K blocks on 1 KB (128-byte swizzle atoms)");
     static constexpr int kTmemNeed = NBUF * BN;
     static constexpr int kTmemCols = kTmemNeed <= 32 ? 32 : kTmemNeed <= 64 ? 64 : kTmemNeed <= 128 ? 128
                                      : kTmemNeed <= 256 ? 256 : 512;
@@ -475,7 +481,7 @@ struct Cfg {
 };
 
 // In-kernel per-1x128 quantization of the bf16 activations (decode) into
-// the resident operand: a K block's codes at a_res + kb*BN*128 in the layout
+// the resident operand: a K block's codes at a_res + kb*1024 (8 rows) in the layout
 // a 128-byte-swizzled TMA copy leaves (row r's 128 codes at r*128, 16-byte
 // chunk c at chunk c ^ (r & 7)); its scales to both scale slots ([kb][row],
 // the second one slot_stride floats on).  Rows past M are zero (codes and
@@ -484,16 +490,18 @@ struct Cfg {
 // four units at a time per warp so that their latency chains (loads,
 // shuffles, the scale division) overlap.  The arithmetic is the norm+quant
 // kernels' (group_quant.cuh).
-// Rows [live, BN) of the resident operand: zero codes (whole 128-byte rows,
-// so the swizzle does not matter) and zero scales.
+// Rows [live, 8) of the resident operand's K blocks: zero codes (whole
+// 128-byte rows, so the swizzle does not matter); rows [live, BN) of the
+// scales: zero.
 template <int BN>
 __device__ __forceinline__ void zero_rows(int KB, int live, uint8_t* a_res, float* sa_slots, int slot_stride, int qw,
                                           int nw, int lane) {
-    const int zero_vec = (BN - live) * (kBK / 16);          // uint4 per K block
+    constexpr int kRows = 8;                                // resident rows per K block
+    const int zero_vec = (live < kRows ? kRows - live : 0) * (kBK / 16);   // uint4 per K block
     for (int e = qw * 32 + lane; e < KB * zero_vec; e += nw * 32) {
         const int kb = e / zero_vec, v = e % zero_vec;
-        if (bounds_ok(kb < KB && live * kBK + 16 * (v + 1) <= BN * kBK))
-            reinterpret_cast<uint4*>(a_res + kb * (BN * kBK) + live * kBK)[v] = make_uint4(0, 0, 0, 0);
+        if (bounds_ok(kb < KB && live * kBK + 16 * (v + 1) <= kRows * kBK))
+            reinterpret_cast<uint4*>(a_res + kb * (kRows * kBK) + live * kBK)[v] = make_uint4(0, 0, 0, 0);
     }
     for (int e = qw * 32 + lane; e < KB * (BN - live); e += nw * 32) {
         const int kb = e / (BN - live), r = live + e % (BN - live);
@@ -508,7 +516,7 @@ __device__ __forceinline__ void quantize_activations(const Params& p, uint8_t* a
                                                      int slot_stride, int qw, int nw, int lane) {
     constexpr int kU = 4;                       // units in flight per warp
     const int KB = p.KB;
-    const int live = p.M < BN ? p.M : BN;
+    const int live = p.M < 8 ? p.M : 8;         // the dispatch bound: at most 8 rows
     zero_rows<BN>(KB, live, a_res, sa_slots, slot_stride, qw, nw, lane);
     const int slots = (KB + 1) / 2;
     const int units = live * slots;
@@ -551,8 +559,8 @@ __device__ __forceinline__ void quantize_activations(const Params& p, uint8_t* a
             uint2 codes = quant8_bracket(x[j], gq, ok);
             if (!ok) codes = quant8_divide(x[j], gq.scale);
             const int r = row[j];
-            if (!bounds_ok(r < BN && kb[j] < KB && kb[j] * BN + r < slot_stride)) continue;
-            *reinterpret_cast<uint2*>(a_res + kb[j] * (BN * kBK) + r * kBK + ((c16 ^ (r & 7)) << 4) + (lane & 1) * 8) =
+            if (!bounds_ok(r < 8 && kb[j] < KB && kb[j] * BN + r < slot_stride)) continue;
+            *reinterpret_cast<uint2*>(a_res + kb[j] * (8 * kBK) + r * kBK + ((c16 ^ (r & 7)) << 4) + (lane & 1) * 8) =
                 codes;
             if ((lane & 15) == 0) {
                 sa_slots[kb[j] * BN + r] = gq.scale;
@@ -583,7 +591,7 @@ __device__ __forceinline__ void norm_quantize_activations(const Params& p, uint8
     constexpr int kMaxSlots = 8;                // 256 columns per slot: K <= 2048
     __shared__ float unit_ssq[16 * kMaxSlots];  // [row][slot], rows < 16 (MMA N = 16)
     const int KB = p.KB;
-    const int live = p.M < BN ? p.M : BN;
+    const int live = p.M < 8 ? p.M : 8;         // the dispatch bound: at most 8 rows
     zero_rows<BN>(KB, live, a_res, sa_slots, slot_stride, qw, nw, lane);
     const int slots = (KB + 1) / 2;
     const int units = live * slots;
@@ -591,7 +599,7 @@ __device__ __forceinline__ void norm_quantize_activations(const Params& p, uint8
     const int c16 = (lane & 15) >> 1;
     const bool side = blockIdx.x == 0;
     const int K = KB * kBK;
-    if (!bounds_ok(units <= kU * nw && slots <= kMaxSlots && live <= 16)) return;   // (debug build) outside the dispatch bound
+    if (!bounds_ok(units <= kU * nw && slots <= kMaxSlots && p.M <= 8)) return;   // (debug build) outside the dispatch bound
 
     int row[kU] = {}, slot[kU] = {};
     bool on[kU] = {}, in[kU] = {};
@@ -646,12 +654,12 @@ __device__ __forceinline__ void norm_quantize_activations(const Params& p, uint8
         for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
         const int m = row[j], kb = 2 * slot[j] + h;
         if (kb >= KB) continue;                 // odd KB: past the row (this half-warp only; no shuffles follow)
-        if (!bounds_ok(m < BN && m < p.M && kb * BN + m < slot_stride)) continue;
+        if (!bounds_ok(m < 8 && m < p.M && kb * BN + m < slot_stride)) continue;
         const GroupQuant gq = make_group_quant(amax);
         bool ok;
         uint2 codes = quant8_bracket(x, gq, ok);
         if (!ok) codes = quant8_divide(x, gq.scale);
-        *reinterpret_cast<uint2*>(a_res + kb * (BN * kBK) + m * kBK + ((c16 ^ (m & 7)) << 4) + (lane & 1) * 8) = codes;
+        *reinterpret_cast<uint2*>(a_res + kb * (8 * kBK) + m * kBK + ((c16 ^ (m & 7)) << 4) + (lane & 1) * 8) = codes;
         if ((lane & 15) == 0) {
             sa_slots[kb * BN + m] = gq.scale;
             sa_slots[slot_stride + kb * BN + m] = gq.scale;
@@ -733,8 +741,8 @@ block_scaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
     // 1024-byte alignment for the 128-byte-swizzled tiles.
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* tiles = smem;
-    uint8_t* a_res = smem + STAGES * C::kStageBytes;          // AQ: [KB][BN rows][128] e4m3, resident
-    uint8_t* out_stage = a_res + (AQ ? p.KB * C::kResBytes : 0);   // [EPI_WARPS][kStageOutBytes]
+    uint8_t* a_res = smem + STAGES * C::kStageBytes;          // AQ: [KB + 1][8 rows][128] e4m3, resident
+    uint8_t* out_stage = a_res + (AQ ? (p.KB + 1) * C::kResBytes : 0);   // [EPI_WARPS][kStageOutBytes]
     uint64_t* bars = reinterpret_cast<uint64_t*>(out_stage + EPI_WARPS * C::kStageOutBytes);
     uint64_t* full = bars;                    // [STAGES] TMA -> MMA
     uint64_t* empty = bars + STAGES;          // [STAGES] MMA -> TMA
@@ -1155,7 +1163,7 @@ template <int BN, bool SWAP, int STAGES, int NBUF, int EPI_WARPS, int AQ = 0>
 constexpr size_t smem_bytes(int KB) {
     using C = Cfg<BN, SWAP, STAGES, NBUF, EPI_WARPS, AQ>;
     const int KBP = (KB + 3) & ~3;
-    return 1024 /* alignment slack */ + STAGES * C::kStageBytes + (AQ ? static_cast<size_t>(KB) * C::kResBytes : 0) +
+    return 1024 /* alignment slack */ + STAGES * C::kStageBytes + (AQ ? static_cast<size_t>(KB + 1) * C::kResBytes : 0) +
            EPI_WARPS * C::kStageOutBytes + (2 * STAGES + 2 * NBUF + 6) * 8 + 16 + 16 +
            static_cast<size_t>(2 * KBP * C::kScaleCols + 2 * KBP) * 4;
 }
@@ -1831,10 +1839,11 @@ struct Consumer {
 // units (measured on GB300 at K=1536, per call in a graph: M=1 11.1 us vs
 // 13.1-13.4 us for the quant kernel then the GEMM, M=6 12.6 vs 13.1-13.4;
 // with the bound raised, M=8 / 12 / 16 took 13.9 / 15.2 / 16.4 us against
-// 13.1-13.4).  At most 16 rows (MMA N=16), K <= 2048.
+// 13.1-13.4).  At most 8 rows (the resident operand's rows per K block),
+// K <= 2048.
 bool bf16a_in_gemm(int64_t M, int64_t K) {
     const int64_t slots = (K / 128 + 1) / 2;
-    return M >= 1 && M <= 16 && K <= 2048 && M * slots <= 40;
+    return M >= 1 && M <= 8 && K <= 2048 && M * slots <= 40;
 }
 
 dsnq_status check_consumer(const Consumer& c, int64_t K) {
@@ -1879,8 +1888,8 @@ size_t variant_smem(int v, int KB) {
         case kVarTile128: return gemm::smem_bytes<128, false, 5, 4, 16>(KB);
         case kVarTile128K: return gemm::smem_bytes<128, false, 3, 4, 16>(KB);
         case kVarPair: return gemm::pair::smem_bytes(KB);
-        case kVarDecodeQuant: return gemm::smem_bytes<16, true, 5, 16, 8, 1>(KB);
-        case kVarDecodeNormQuant: return gemm::smem_bytes<16, true, 5, 16, 8, 2>(KB);
+        case kVarDecodeQuant: return gemm::smem_bytes<16, true, 6, 2, 8, 1>(KB);
+        case kVarDecodeNormQuant: return gemm::smem_bytes<16, true, 5, 2, 8, 2>(KB);
     }
     return 0;
 }
@@ -2096,12 +2105,17 @@ dsnq_status run_gemm(int64_t M, int64_t K, const void* a, int64_t lda, const flo
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     switch (variant) {
         // Decode on bf16 activations quantized (and normalized) in the
-        // prologue: two CTAs per SM like the 16-token decode variant (five
-        // stages, half of TMEM each), so that all 224 weight tiles stream in
-        // one wave (M=1: 14.1 -> 11.1 us per call in a graph; with one CTA
-        // per SM, eight stages, 72 SMs took a second tile).
-        case kVarDecodeQuant: return launch<16, true, 5, 16, 8, 1, 2>(prm, ma, mw[0], mw[1], mo[0], mo[1], s);
-        case kVarDecodeNormQuant: return launch<16, true, 5, 16, 8, 2, 2>(prm, ma, mw[0], mw[1], mo[0], mo[1], s);
+        // prologue: two CTAs per SM like the 16-token decode variant, so
+        // that all 224 weight tiles stream in one wave (M=1: 14.1 -> 11.1 us
+        // per call in a graph; with one CTA per SM, eight stages, 72 SMs
+        // took a second tile).  The 8-row resident operand leaves room for
+        // a sixth stage; two TMEM buffers suffice at these sizes.  Measured
+        // per call in graphs of 100 at M=1 against five stages, sixteen
+        // buffers and a 16-row operand: quantize only 10.33 -> 9.92-9.94 us,
+        // norm+quant 11.17-11.19 -> 10.99-11.01 us (a sixth stage there:
+        // 11.41 us).
+        case kVarDecodeQuant: return launch<16, true, 6, 2, 8, 1, 2>(prm, ma, mw[0], mw[1], mo[0], mo[1], s);
+        case kVarDecodeNormQuant: return launch<16, true, 5, 2, 8, 2, 2>(prm, ma, mw[0], mw[1], mo[0], mo[1], s);
         case kVarPair: return launch_pair(prm, ma, mw[0], mw[1], mo[0], mo[1], s);
         // Decode: the kernel streams the weights.  Up to 32 tokens two CTAs
         // share an SM (five stages, half of TMEM each), so that all 224

@@ -301,7 +301,7 @@ DSNQ_API dsnq_status dsnq_bf16a_workspace_bytes(int64_t M, int64_t K, int64_t* c
  *   a_fp8_ws, a_scale_ws : caller-owned workspace for the quantized pair,
  *                 M*K bytes (16-byte aligned) and M*(K/128) floats (4-byte
  *                 aligned, written column-major).  Unused, and may be NULL,
- *                 when M <= 16, K <= 2048 and M * ceil(K/256) <= 40 (M <= 6
+ *                 when M <= 8, K <= 2048 and M * ceil(K/256) <= 40 (M <= 6
  *                 at K = 1536): there one launch quantizes the activations
  *                 inside the GEMM, into shared memory.  Every CTA quantizes
  *                 all M rows, so larger batches run the quant kernel into the
@@ -348,7 +348,7 @@ DSNQ_API dsnq_status dsnq_block_scaled_fp8_gemm_dual_bf16a_static(
  * GEMM of dsnq_block_scaled_fp8_gemm_dual on the quantized q latent.  Same
  * formulas; kv_out as in the fused call.  No counterpart in the published
  * method, which launches the two steps separately: for a few decode rows
- * (M <= 16, Kq <= 2048, Kkv <= 2048 and M * ceil(Kq/256) <= 40, i.e. M <= 6
+ * (M <= 8, Kq <= 2048, Kkv <= 2048 and M * ceil(Kq/256) <= 40, i.e. M <= 6
  * at Kq = 1536) one launch normalizes and quantizes the rows inside the GEMM,
  * where both steps are bound by latency; otherwise the fused norm+quant
  * kernel writes (q_fp8, q_scale) and the GEMM reads them.
