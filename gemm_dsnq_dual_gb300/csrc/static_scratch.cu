@@ -39,8 +39,15 @@ bool scratch_ptrs(ScratchPtrs* out) {
         std::lock_guard<std::mutex> lk(g_lock);
         if (!g_ready[dev].load(std::memory_order_relaxed)) {
             ScratchPtrs p{};
-            if (cudaGetSymbolAddress(&p.codes, g_scratch_codes) != cudaSuccess ||
-                cudaGetSymbolAddress(reinterpret_cast<void**>(&p.scales), g_scratch_scales) != cudaSuccess) {
+            // The lookup may load the library's device code; in relaxed
+            // capture mode for this thread it is allowed while a stream of
+            // the caller is being captured (the first call inside a graph).
+            cudaStreamCaptureMode mode = cudaStreamCaptureModeRelaxed;
+            cudaThreadExchangeStreamCaptureMode(&mode);
+            const bool found = cudaGetSymbolAddress(&p.codes, g_scratch_codes) == cudaSuccess &&
+                               cudaGetSymbolAddress(reinterpret_cast<void**>(&p.scales), g_scratch_scales) == cudaSuccess;
+            cudaThreadExchangeStreamCaptureMode(&mode);   // the caller's mode back
+            if (!found) {
                 cudaGetLastError();
                 return false;
             }

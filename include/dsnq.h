@@ -331,7 +331,8 @@ DSNQ_API dsnq_status dsnq_block_scaled_fp8_gemm_dual_bf16a(
  * outside the one-launch case) share it: on one device they must be ordered,
  * e.g. issued to one stream, since calls that overlap on the GPU race on it.
  * The first call on a device looks the array's address up (which may load
- * the library's device code); make that first call before any stream capture.
+ * the library's device code), in relaxed capture mode for the calling thread,
+ * so that first call may also be made while a stream is being captured.
  */
 DSNQ_API dsnq_status dsnq_block_scaled_fp8_gemm_dual_bf16a_static(
     int64_t M, int64_t K,
