@@ -68,11 +68,13 @@ def test_matches_oracle(M):
     assert torch.equal(o1, t1) and torch.equal(o2, t2)
 
 
-@pytest.mark.parametrize("M,Kq", [(1, 1408), (3, 1408), (6, 1408), (1, 2048), (2, 2048), (5, 512)])
+@pytest.mark.parametrize("M,Kq", [(1, 1408), (3, 1408), (6, 1408), (1, 2048), (2, 2048), (5, 512), (8, 512),
+                                  (8, 1280), (7, 1024)])
 def test_one_launch_other_widths(M, Kq):
     """The one-launch route at other q widths: an odd number of K blocks (the
     last 256-column unit half past the row), the widest row it takes (eight
-    units), and a narrow one; one to six rows spread over the quantizer warps."""
+    units), and a narrow one; one to eight rows (all of the resident operand's
+    rows) spread over the quantizer warps."""
     assert dsnq.fused_quant_fits(M, Kq)
     g = torch.Generator().manual_seed(90 + M + Kq)
     q = (torch.randn(M, Kq, generator=g) * 2.0).to(torch.bfloat16)

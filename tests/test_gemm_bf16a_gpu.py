@@ -39,7 +39,9 @@ SHAPES = [
     (1, 1536, 512, 256),    # quantized inside the GEMM ...
     (6, 1536, 256, 128),
     (5, 384, 256, 0),       # odd number of K blocks
-    (16, 128, 128, 128),    # one K block, 16 rows
+    (16, 128, 128, 128),    # one K block, 16 rows (two launches: more than 8 rows)
+    (8, 128, 128, 128),     # one K block, 8 rows: every resident row live, the MMA's rows 8..15 in the spare block
+    (8, 1280, 256, 128),    # 8 rows x 5 slots = 40 units: the in-GEMM bound
     (2, 2048, 256, 0),      # largest K quantized in the GEMM
     (7, 1536, 512, 256),    # ... and the quant kernel, then the GEMM
     (17, 1536, 512, 256),
