@@ -882,7 +882,8 @@ def run_kernel_only(args):
     norm+quant, `single_latent` the single-latent norm+quant of q,
     `unfused` the unfused baseline's three launches (norm to bf16, then the
     quant of q twice), `fused_step` the one-launch norm+quant+GEMM (a few
-    decode rows); no timing, no JSON line.  Every mode first runs one fused
+    decode rows), `bf16a` the dual GEMM on the bf16 q rows (quantized inside
+    the GEMM for a few rows); no timing, no JSON line.  Every mode first runs one fused
     norm+quant to make its inputs."""
     import torch
     import gemm_dsnq_dual_gb300 as dsnq
@@ -893,7 +894,7 @@ def run_kernel_only(args):
     q, kv = lat.q.to(dev), lat.kv.to(dev)
     gq, gkv = lat.gamma_q.to(dev), lat.gamma_kv.to(dev)
     q8, s8, _ = dsnq.fused_dual_rmsnorm_group_quant(q, kv, gq, gkv, lat.eps, scale_layout="col")
-    if args.kernel_only in ("gemm", "fused_step"):
+    if args.kernel_only in ("gemm", "fused_step", "bf16a"):
         wa, swa = dsnq.quantize_weight_block128(inputs.weight(N_ATTN, KQ, seed=0, salt=1).to(dev))
         wi, swi = dsnq.quantize_weight_block128(inputs.weight(N_IDX, KQ, seed=0, salt=2).to(dev))
     if args.kernel_only == "gemm":
@@ -901,6 +902,8 @@ def run_kernel_only(args):
     elif args.kernel_only == "fused_step":
         # The decode step as one launch (norm+quant inside the GEMM's prologue).
         fn = lambda: dsnq.fused_norm_quant_gemm_dual(q, kv, gq, gkv, lat.eps, wa, swa, wi, swi)
+    elif args.kernel_only == "bf16a":
+        fn = lambda: dsnq.block_scaled_fp8_gemm_dual_bf16a(q, wa, swa, wi, swi)
     elif args.kernel_only == "single_latent":
         fn = lambda: dsnq.rmsnorm_group_quant(q, gq, lat.eps, scale_layout="col", x_out=q8, x_scale=s8)
     elif args.kernel_only == "unfused":
@@ -935,7 +938,7 @@ def main():
     ap.add_argument("--no-long-context", dest="long_context", action="store_false",
                     help="skip the M=32768 long-context GEMM of the side measurements")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--kernel-only", choices=["gemm", "norm_quant", "single_latent", "unfused", "fused_step"],
+    ap.add_argument("--kernel-only", choices=["gemm", "norm_quant", "single_latent", "unfused", "fused_step", "bf16a"],
                     default=None,
                     help="profiling aid: launch one kernel --launches times and exit")
     ap.add_argument("--launches", type=int, default=3)
